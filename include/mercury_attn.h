@@ -1,0 +1,182 @@
+/*
+ * mercury_attn.h -- C ABI of the GB300 (sm_103a) shifted-schedule sharded
+ * attention library (libmercury_attn.so).
+ *
+ * The operation.  Mercury (SOSP 2025) keeps a shared KV buffer sharded across
+ * ranks and lets every rank consume the shards in a rank-staggered order
+ * instead of all at once (Silicon & Systems, "The hidden cost of synchronized
+ * operators"); its shift primitive gives rank i at step j the piece
+ * (j + i) mod J (Mercury-SOSP25 paper notes, section 核心方法).  The local
+ * computation at every step is a fixed attention "patch" (FlashAttention) and
+ * its result must equal single-device attention (Silicon & Systems,
+ * "CommIR makes communication transformable" and "The tuning bill").
+ *
+ * Here R virtual ranks live in one GPU's memory.  Queries are split into R
+ * contiguous blocks of Sq/R rows and keys/values into R contiguous shards of
+ * Skv/R rows; virtual rank i owns query block i and, at step j, attends to KV
+ * shard order[i][j] (see mercury_plan_shift).  The result equals
+ *     O = softmax(Q K^T / sqrt(d)) V,   LSE = ln sum_k exp(q.k / sqrt(d))
+ * for MHA, GQA and MQA (query head h uses KV head h / (Hq/Hkv)), causal
+ * (key k allowed for query q iff k <= q + Skv - Sq) or not.
+ *
+ * Conventions for every call below.
+ *   - Tensors are device pointers, row-major and contiguous, allocated and
+ *     owned by the caller; the library keeps no reference after a call
+ *     returns.  q [B,Hq,Sq,d] bf16; k, v [B,Hkv,Skv,d] bf16;
+ *     out [B,Hq,Sq,d] fp32; lse [B,Hq,Sq] fp32 (natural log).
+ *   - bf16 inputs and fp32 outputs must be 16-byte aligned (TMA and vector
+ *     stores need it); lse arrays 4-byte aligned.
+ *   - stream is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Compute calls are asynchronous on that stream.
+ *   - Return value: MERCURY_OK (0) or a negative status; the message of the
+ *     last non-zero status of the calling thread is mercury_last_error().
+ *     No call throws, exits or traps.
+ *   - Device waits are bounded (2 s by default, env MERCURY_WAIT_NS).  A wait
+ *     that runs out makes the kernel record MERCURY_ETIMEOUT in a device
+ *     error word and return early; that status is reported by
+ *     mercury_sync_status().  With env MERCURY_SYNC_CHECK=1 every compute
+ *     call synchronises its stream and returns the status itself.
+ */
+#ifndef MERCURY_ATTN_H
+#define MERCURY_ATTN_H
+
+#if defined(__GNUC__)
+#define MERCURY_API __attribute__((visibility("default")))
+#else
+#define MERCURY_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MERCURY_OK        0
+#define MERCURY_EINVAL   (-1)  /* bad argument: null pointer, bad size, bad shift, ... */
+#define MERCURY_EALIGN   (-2)  /* a pointer is not aligned as required              */
+#define MERCURY_ECUDA    (-3)  /* CUDA runtime / driver error (message has details) */
+#define MERCURY_ETIMEOUT (-4)  /* a bounded device wait ran out                     */
+#define MERCURY_ENOMEM   (-5)  /* host-side allocation failed                       */
+
+/* Largest number of virtual ranks a compute call accepts. */
+#define MERCURY_MAX_R 128
+
+/*
+ * mercury_plan_shift -- the shard/shift planner (pure host code, no GPU).
+ *
+ * Writes the [R][R] table order[i*R + j] = KV shard that virtual rank i reads
+ * at step j.  shift selects the order:
+ *   0      unshifted: order[i][j] = j (every rank reads the same shard at the
+ *          same step: the synchronous, replicated schedule);
+ *   1      flat shift: order[i][j] = (i + j) mod R, the shift primitive's
+ *          "(j+i)%J" access (Mercury-SOSP25 paper notes, 核心方法);
+ *   k >= 2 nested two-level shift for an Ro x Ri mesh with Ri = k inner
+ *          (fast-link) ranks and Ro = R / k outer groups (hierarchical 2x4 /
+ *          4x2 topologies, Silicon & Systems "What Mercury finds that
+ *          templates miss"): rank i = a*Ri + b, step j = s*Ri + t,
+ *          order = ((a + s) mod Ro)*Ri + (b + t) mod Ri.  k must divide R;
+ *          k = R gives the flat order.
+ * Every row and every column of the table is a permutation of 0..R-1.
+ * order: host array of R*R ints, caller-owned.
+ * Errors: MERCURY_EINVAL if R < 1, R > MERCURY_MAX_R, shift < 0, k does not
+ * divide R, or order is NULL.
+ */
+MERCURY_API int mercury_plan_shift(int R, int shift, int *order);
+
+/*
+ * mercury_attn_sharded -- full attention through the shifted schedule, with
+ * the per-step partials combined on the fly (online softmax across steps, the
+ * same arithmetic as a log-sum-exp merge taken in step order).
+ *
+ * Virtual rank i processes its query block against shards order[i][0..R-1]
+ * (mercury_plan_shift(R, shift)); under causal masking a shard entirely in the
+ * future of a block is skipped and the diagonal shard is masked per element.
+ * Writes out [B,Hq,Sq,d] fp32 and lse [B,Hq,Sq] fp32.
+ * Requirements: B, Hq, Hkv, Sq, Skv >= 1; Hq % Hkv == 0; d in {64, 128};
+ * 1 <= R <= MERCURY_MAX_R; Sq % R == 0 and Skv % R == 0; causal requires
+ * Sq <= Skv; valid shift (as in mercury_plan_shift); every element count fits
+ * in 63 bits and every sequence / head coordinate in 31 bits.
+ * Errors: MERCURY_EINVAL, MERCURY_EALIGN, MERCURY_ECUDA, and
+ * MERCURY_ETIMEOUT when MERCURY_SYNC_CHECK=1.
+ */
+MERCURY_API int mercury_attn_sharded(const void *q, const void *k, const void *v,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                         int R, int shift, int causal,
+                         float *out, float *lse, void *stream);
+
+/*
+ * mercury_attn_partial -- the per-step partials of the shifted schedule.
+ *
+ * For every query row q (virtual rank i = q / (Sq/R)) and step j, slot j of
+ * the outputs holds attention of that row over shard order[i][j] alone,
+ * normalised within the shard:
+ *   o_part  [R][B,Hq,Sq,d] fp32, lse_part [R][B,Hq,Sq] fp32.
+ * A row with no allowed key in its shard (causal) gets O = 0, LSE = -inf.
+ * mercury_lse_merge(o_part, lse_part, R, B*Hq*Sq, d, out, lse) then gives the
+ * same result as mercury_attn_sharded.  Requirements and errors as for
+ * mercury_attn_sharded.
+ */
+MERCURY_API int mercury_attn_partial(const void *q, const void *k, const void *v,
+                         int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                         int R, int shift, int causal,
+                         float *o_part, float *lse_part, void *stream);
+
+/*
+ * mercury_lse_merge -- exact log-sum-exp combine of n_parts partial results.
+ *
+ * Per row r:  L = ln sum_j exp(lse_part[j][r]),
+ *             out[r][:] = sum_j exp(lse_part[j][r] - L) * o_part[j][r][:],
+ *             lse[r] = L.
+ * A part with lse = -inf has weight 0 and its o_part row is not read; a row
+ * whose parts are all -inf gets out = 0 and lse = -inf.  The pages name no
+ * combine formula; this is the standard exact one of the RingAttention-style
+ * schedules that Mercury reproduces (Mercury-SOSP25 paper notes, one-line
+ * summary).
+ * o_part [n_parts][rows][d] fp32 (16-byte aligned), lse_part [n_parts][rows]
+ * fp32, out [rows][d] fp32 (16-byte aligned), lse [rows] fp32.
+ * Requirements: 1 <= n_parts <= 4096; rows >= 0; d % 4 == 0, 4 <= d <= 512;
+ * n_parts*rows*d fits in 63 bits.  rows == 0 is a no-op.
+ * Errors: MERCURY_EINVAL, MERCURY_EALIGN, MERCURY_ECUDA.
+ */
+MERCURY_API int mercury_lse_merge(const float *o_part, const float *lse_part, int n_parts,
+                      long long rows, int d, float *out, float *lse, void *stream);
+
+/*
+ * mercury_sync_status -- synchronise `stream`, then read and clear the device
+ * error word of this process's kernels.  Returns MERCURY_OK,
+ * MERCURY_ETIMEOUT (a bounded device wait ran out in some earlier kernel) or
+ * MERCURY_ECUDA (the synchronise itself failed).
+ */
+MERCURY_API int mercury_sync_status(void *stream);
+
+/* Message for the last non-zero status returned to the calling thread
+ * ("" if none).  The pointer stays valid until the thread's next call. */
+MERCURY_API const char *mercury_last_error(void);
+
+/*
+ * mercury_work_decomposition -- host-side view of how a compute call splits
+ * the work (no GPU needed; used to test the planner's coverage).
+ * info[0..7] receives: rows per head in a query tile (Mq), heads per tile
+ * (Gp), pairing mode (1: the two tiles of a work item are two head groups at
+ * the same rows; 0: two consecutive row tiles of the same heads), head tiles
+ * per KV group, row tiles per query block, work items per (batch, KV head,
+ * rank), total work items, 0.  partial selects mercury_attn_partial's split.
+ * Errors: MERCURY_EINVAL for arguments a compute call would reject.
+ */
+MERCURY_API int mercury_work_decomposition(int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                               int R, int causal, int partial, long long *info);
+
+/*
+ * mercury_work_item_rows -- for work item `item` of that decomposition, writes
+ * the flat rows ((b*Hq + h)*Sq + q) it computes and the step it writes
+ * (partial) or -1 (sharded): rows[0..n-1], *n_rows = n (at most 256), *step.
+ * Pure host code, for coverage tests.  Errors: MERCURY_EINVAL.
+ */
+MERCURY_API int mercury_work_item_rows(int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                           int R, int shift, int causal, int partial,
+                           long long item, long long *rows, int *n_rows, int *step);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MERCURY_ATTN_H */

@@ -1,0 +1,625 @@
+// attn_fwd.cu -- the attention "patch" of the shifted schedule on sm_103a.
+//
+// Mercury keeps an optimised local attention kernel fixed and schedules the
+// distributed loop around it (Silicon & Systems, "CommIR makes communication
+// transformable"; Mercury-SOSP25 paper notes 核心方法, FlashAttention patch).
+// This file is that patch for one GB300: a FlashAttention-style forward pass
+// whose KV loop walks the shards in the shifted order, rank i reading shard
+// order[i][j] at step j (the (j+i)%J access of the shift primitive, or its
+// nested two-level form), with the R virtual ranks' data all in local HBM.
+//
+// Per CTA (one work item, up to two 128-row query tiles sharing a KV head):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into two
+//               shared-memory rings, in the shifted shard order
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V on
+//               the tensor cores (tcgen05.mma kind::f16, fp32 accumulators in
+//               tensor memory); P_t is read straight from tensor memory
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (one query row per
+//               thread): online softmax in the log2 domain, rescaling of O_t
+//               in tensor memory when the running max moves by more than
+//               2^8, bf16 P_t written back over S_t, final O/l and LSE
+// Tensor memory (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D)
+// O_1 [256+D, 256+2D).
+//
+// The MMA issue order is PV_0(n-1), S_0(n), PV_1(n-1), S_1(n): the tensor
+// pipe runs one tile's products while the other tile's softmax works.  A
+// commit after S_t(n) therefore also covers PV_t(n-1), so the softmax may
+// rescale O_t as soon as S_t(n) is ready.
+//
+// Every wait is bounded (%globaltimer); when one runs out the CTA records
+// MERCURY_ETIMEOUT in a device error word, raises a shared abort flag so the
+// other roles stop waiting too, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "work.h"
+
+namespace mercury {
+
+// Device error word: bit 0 = a bounded wait ran out.  g_err_site keeps the
+// first site that timed out (for the error message).
+__device__ unsigned int g_err_word = 0;
+__device__ unsigned int g_err_site = 0;
+
+struct AttnParams {
+    Geom g;
+    float scale_log2;        // log2(e) / sqrt(d)
+    int fault;               // test hook: 1 = drop the first P-ready arrive of tile 0
+    float *out;              // fused: out; partial: o_part
+    float *lse;              // fused: lse; partial: lse_part
+    long long slot_o;        // partial: elements between slots of o_part
+    long long slot_lse;      // partial: elements between slots of lse_part
+    unsigned long long wait_ns;
+    // fused: tab[i*R + j] = shard of rank i at step j;
+    // partial: tab[i*R + s] = step (slot) at which rank i reads shard s.
+    unsigned char tab[kMaxR * kMaxR];
+};
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 2^8
+
+struct Ctl {
+    unsigned long long budget;
+    volatile uint32_t *abort;
+};
+
+// Bounded wait on an mbarrier phase.  false: timed out here or elsewhere.
+__device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Ctl c, uint32_t site)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.budget) {
+            *c.abort = 1u;
+            atomicOr(&g_err_word, 1u);
+            atomicCAS(&g_err_site, 0u, site);
+            return false;
+        }
+    }
+}
+
+// Shard visited at step `step` of the item's sequence (fused: R steps;
+// partial: one step, the item's shard).
+__device__ __forceinline__ int shard_at(const AttnParams &p, const Item &it, int step)
+{
+    return p.g.partial ? it.shard : (int)p.tab[it.rank * p.g.R + step];
+}
+
+__device__ __forceinline__ int n_steps(const AttnParams &p)
+{
+    return p.g.partial ? 1 : p.g.R;
+}
+
+template <int D, int NK, int NV>
+struct Smem {
+    static constexpr int kQBytes = kTileRows * D * 2;   // one query tile, bf16
+    static constexpr int kKVBytes = kTileKeys * D * 2;  // one K or V tile, bf16
+    static constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 B swizzle column
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = 2 * kQBytes;
+    static constexpr int kOffV = kOffK + NK * kKVBytes;
+    static constexpr int kOffBar = kOffV + NV * kKVBytes;
+    static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 6;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+template <int D, int NK, int NV>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
+{
+    using L = Smem<D, NK, NV>;
+    constexpr int NBOX = D / 64;  // 128-byte swizzle columns per row
+    // tensor-memory columns of S_t and O_t
+    auto col_s = [](int t) { return (uint32_t)(t * 128); };
+    auto col_o = [](int t) { return (uint32_t)(256 + t * D); };
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTileKeys, false);
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sQ = smem + L::kOffQ;
+    uint8_t *sK = smem + L::kOffK;
+    uint8_t *sV = smem + L::kOffV;
+    uint64_t *bars = (uint64_t *)(smem + L::kOffBar);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + NK;
+    uint64_t *v_full = k_empty + NK;
+    uint64_t *v_empty = v_full + NV;
+    uint64_t *s_full = v_empty + NV;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_full = p_full + 2;
+    uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const Item it = decode_item(p.g, blockIdx.x);
+    const int ntile = it.t[1].valid ? 2 : 1;
+    const Ctl ctl{p.wait_ns, abort_flag};
+
+    // Total KV tiles of the item's shifted sequence.
+    int n_total = 0;
+    for (int st = 0; st < n_steps(p); ++st) {
+        int lo, hi;
+        shard_range(p.g, it, shard_at(p, it, st), lo, hi);
+        n_total += n_kv_tiles(lo, hi);
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(k_full + i, 1);
+            mbar_init(k_empty + i, 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(v_full + i, 1);
+            mbar_init(v_empty + i, 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(s_full + t, 1);
+            mbar_init(p_full + t, 128);
+            mbar_init(o_full + t, 1);
+        }
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0 && n_total > 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQBytes));
+            for (int t = 0; t < ntile; ++t)
+                for (int c = 0; c < NBOX; ++c)
+                    tma_load_3d(sQ + t * L::kQBytes + c * L::kBoxBytes, &tmQ, q_full, c * 64,
+                                it.t[t].q0, it.b * p.g.Hq + it.t[t].h0);
+            const int bkv = it.b * p.g.Hkv + it.hkv;
+            int n = 0;
+            bool ok = true;
+            for (int st = 0; st < n_steps(p) && ok; ++st) {
+                int lo, hi;
+                shard_range(p.g, it, shard_at(p, it, st), lo, hi);
+                const int nt = n_kv_tiles(lo, hi);
+                for (int tt = 0; tt < nt; ++tt, ++n) {
+                    const int k0 = lo + tt * kTileKeys;
+                    const int sk = n % NK;
+                    if (n >= NK && !wait_phase(k_empty + sk, ((n / NK) - 1) & 1, ctl, 0x101)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(k_full + sk, (uint32_t)L::kKVBytes);
+                    for (int c = 0; c < NBOX; ++c)
+                        tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk,
+                                    c * 64, k0, bkv);
+                    const int sv = n % NV;
+                    if (n >= NV && !wait_phase(v_empty + sv, ((n / NV) - 1) & 1, ctl, 0x102)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full + sv, (uint32_t)L::kKVBytes);
+                    for (int c = 0; c < NBOX; ++c)
+                        tma_load_3d(sV + sv * L::kKVBytes + c * L::kBoxBytes, &tmV, v_full + sv,
+                                    c * 64, k0, bkv);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_total > 0) {
+            const uint32_t q_base = smem_u32(sQ);
+            const uint32_t k_base = smem_u32(sK);
+            const uint32_t v_base = smem_u32(sV);
+            // S_t = Q_t K^T over K = D: 16 elements (32 bytes) per MMA inside a
+            // 128-byte swizzle column; 8-row groups 1024 bytes apart.
+            auto issue_qk = [&](int t, int sk) {
+                const uint32_t qa = q_base + t * L::kQBytes;
+                const uint32_t kb = k_base + sk * L::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
+                    umma_ss(tmem + col_s(t), smem_desc_sw128(qa + off, 16, 1024),
+                            smem_desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t += P_t V over K = 128 keys: P_t from tensor memory (bf16 pairs,
+            // 8 columns per 16 keys); V is MN-major (d contiguous): 16 keys =
+            // two 8-row groups = 2048 bytes; the two 64-wide d halves are
+            // kBoxBytes apart (leading-dimension offset).
+            auto issue_pv = [&](int t, int sv, bool acc_in) {
+                const uint32_t vb = v_base + sv * L::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+                    umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
+                            smem_desc_sw128(vb + kk * 2048, L::kBoxBytes, 1024), kIdescPV,
+                            (acc_in || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = wait_phase(q_full, 0, ctl, 0x201);
+            tc_fence_after();
+            int n = 0;
+            for (; n < n_total && ok; ++n) {
+                const int sk = n % NK;
+                if (!wait_phase(k_full + sk, (n / NK) & 1, ctl, 0x202)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (n > 0) {
+                    const int sv = (n - 1) % NV;
+                    for (int t = 0; t < ntile && ok; ++t) {
+                        if (!wait_phase(p_full + t, (n - 1) & 1, ctl, 0x203)) {
+                            ok = false;
+                            break;
+                        }
+                        if (t == 0 && !wait_phase(v_full + sv, ((n - 1) / NV) & 1, ctl, 0x204)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, sv, n - 1 > 0);
+                        issue_qk(t, sk);
+                        umma_commit(s_full + t);
+                    }
+                    if (!ok)
+                        break;
+                    umma_commit(v_empty + sv);
+                } else {
+                    for (int t = 0; t < ntile; ++t) {
+                        issue_qk(t, sk);
+                        umma_commit(s_full + t);
+                    }
+                }
+                umma_commit(k_empty + sk);
+            }
+            if (ok) {
+                const int last = n_total - 1;
+                const int sv = last % NV;
+                for (int t = 0; t < ntile && ok; ++t) {
+                    if (!wait_phase(p_full + t, last & 1, ctl, 0x205)) {
+                        ok = false;
+                        break;
+                    }
+                    if (t == 0 && !wait_phase(v_full + sv, (last / NV) & 1, ctl, 0x206)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(t, sv, last > 0);
+                    umma_commit(o_full + t);
+                }
+                if (ok) {
+                    umma_commit(v_empty + sv);
+                    // Drain: let the last release of every ring stage land before
+                    // the CTA's shared memory goes away.
+                    for (int m = (n_total > NK ? n_total - NK : 0); m < n_total && ok; ++m)
+                        ok = wait_phase(k_empty + (m % NK), (m / NK) & 1, ctl, 0x207);
+                    for (int m = (n_total > NV ? n_total - NV : 0); m < n_total && ok; ++m)
+                        ok = wait_phase(v_empty + (m % NV), (m / NV) & 1, ctl, 0x208);
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- softmax
+        const int t = (warp - 4) / 4;
+        const int quarter = warp % 4;  // tcgen05.ld lane quarter of this warp
+        const int r = quarter * 32 + lane;
+        if (t < ntile) {
+            const Tile &T = it.t[t];
+            const int head = T.h0 + r / p.g.Mq;
+            const int qi = T.q0 + r % p.g.Mq;
+            const bool row_valid = (r % p.g.Mq) < T.nq;
+            const long long causal_lim =
+                p.g.causal ? (long long)qi + (p.g.Skv - p.g.Sq) : (long long)p.g.Skv;
+            const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
+            const uint32_t tS = tmem + lane_field + col_s(t);
+            const uint32_t tO = tmem + lane_field + col_o(t);
+            const float scale = p.scale_log2;
+            float m = -INFINITY;  // running max (log2 domain), possibly stale by < 2^8
+            float l = 0.f;        // running sum of 2^(y - m)
+            bool ok = true;
+            int n = 0;
+            for (int st = 0; st < n_steps(p) && ok; ++st) {
+                int lo, hi;
+                shard_range(p.g, it, shard_at(p, it, st), lo, hi);
+                const int nt = n_kv_tiles(lo, hi);
+                for (int tt = 0; tt < nt; ++tt, ++n) {
+                    const int k0 = lo + tt * kTileKeys;
+                    // allowed columns c: k0 + c < hi and k0 + c <= causal limit
+                    long long lim = (long long)hi - 1;
+                    if (causal_lim < lim)
+                        lim = causal_lim;
+                    lim -= k0;
+                    bool got = wait_phase(s_full + t, n & 1, ctl, 0x301);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t sr[128];
+                    tmem_ld_x128(tS, sr);
+                    float *s = reinterpret_cast<float *>(sr);
+                    if (lim < kTileKeys - 1) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (c > lim)
+                                s[c] = -INFINITY;
+                    }
+                    float mx = s[0];
+#pragma unroll
+                    for (int c = 1; c < 128; ++c)
+                        mx = fmaxf(mx, s[c]);
+                    const float m_cand = fmaxf(m, mx * scale);
+                    const bool need = (m == -INFINITY) ? (m_cand != -INFINITY)
+                                                       : (m_cand - m > kRescaleThreshold);
+                    const float m_new = need ? m_cand : m;
+                    __syncwarp();
+                    if (n > 0 && __any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+                        l *= alpha;
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                            tmem_st_x32(tO + c0, o);
+                        }
+                    }
+                    m = m_new;
+                    const float mu = (m == -INFINITY) ? 0.f : m;
+                    float sum = 0.f;
+                    uint32_t pk[64];
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const float p0 = ex2_approx(fmaf(s[2 * c], scale, -mu));
+                        const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale, -mu));
+                        sum += p0 + p1;
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);  // low half = p0
+                        pk[c] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    l += sum;
+                    uint32_t pa[32], pb[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        pa[c] = pk[c];
+                        pb[c] = pk[32 + c];
+                    }
+                    tmem_st_x32(tS, pa);
+                    tmem_st_x32(tS + 32, pb);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    if (!(p.fault == 1 && t == 0 && n == 0))
+                        mbar_arrive(p_full + t);
+                }
+            }
+            // ------------------------------------------------- epilogue
+            float *orow = nullptr;
+            float *lrow = nullptr;
+            if (row_valid) {
+                long long row = ((long long)it.b * p.g.Hq + head) * p.g.Sq + qi;
+                long long so = 0, sl = 0;
+                if (p.g.partial) {
+                    const int slot = p.tab[it.rank * p.g.R + it.shard];
+                    so = slot * p.slot_o;
+                    sl = slot * p.slot_lse;
+                }
+                orow = p.out + so + row * D;
+                lrow = p.lse + sl + row;
+            }
+            if (ok && n_total > 0) {
+                bool got = wait_phase(o_full + t, 0, ctl, 0x302);
+                ok = __all_sync(0xffffffffu, got);
+                if (ok) {
+                    tc_fence_after();
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld_x32(tO + c0, o);
+                        if (orow) {
+                            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv,
+                                                     __uint_as_float(o[4 * c + 1]) * inv,
+                                                     __uint_as_float(o[4 * c + 2]) * inv,
+                                                     __uint_as_float(o[4 * c + 3]) * inv);
+                        }
+                    }
+                    if (lrow)
+                        *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                }
+            } else if (n_total == 0 && orow) {
+                // no allowed key for any row of this item in this shard
+                float4 *dst = reinterpret_cast<float4 *>(orow);
+                for (int c = 0; c < D / 4; ++c)
+                    dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                *lrow = -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode_fn(char *msg, size_t msg_len)
+{
+    static EncodeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = (EncodeFn)ptr;
+    }
+    if (!fn)
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
+    return fn;
+}
+
+// 3-D bf16 tensor [d2][d1][d0] (d0 innermost), 128-byte swizzle, zero fill.
+int encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+              uint32_t b1, uint32_t b2, char *msg, size_t msg_len)
+{
+    EncodeFn fn = get_encode_fn(msg, msg_len);
+    if (!fn)
+        return MERCURY_ECUDA;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+        return MERCURY_ECUDA;
+    }
+    return MERCURY_OK;
+}
+
+template <int D, int NK, int NV>
+int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                cudaStream_t stream, char *msg, size_t msg_len)
+{
+    using L = Smem<D, NK, NV>;
+    auto kern = attn_fwd_kernel<D, NK, NV>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            return MERCURY_ECUDA;
+        }
+        attr_set = true;
+    }
+    if (p.g.n_items > 0x7fffffffLL) {
+        snprintf(msg, msg_len, "too many work items (%lld)", p.g.n_items);
+        return MERCURY_EINVAL;
+    }
+    kern<<<(unsigned)p.g.n_items, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "attention kernel launch: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    return MERCURY_OK;
+}
+
+}  // namespace
+
+int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len)
+{
+    // The parameter block (16 KB of shift table) lives in thread-local
+    // storage: the launch path makes no heap allocation.
+    static thread_local AttnParams p;
+    memset(&p, 0, sizeof p);
+    if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.partial)) {
+        snprintf(msg, msg_len, "unsupported shape");
+        return MERCURY_EINVAL;
+    }
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
+    p.fault = c.fault;
+    p.out = c.out;
+    p.lse = c.lse;
+    p.slot_o = (long long)c.B * c.Hq * c.Sq * c.d;
+    p.slot_lse = (long long)c.B * c.Hq * c.Sq;
+    p.wait_ns = c.wait_ns;
+    const int R = c.R;
+    for (int i = 0; i < R; ++i)
+        for (int j = 0; j < R; ++j) {
+            const int s = c.order[i * R + j];
+            if (c.partial)
+                p.tab[i * R + s] = (unsigned char)j;
+            else
+                p.tab[i * R + j] = (unsigned char)s;
+        }
+    CUtensorMap mq, mk, mv;
+    int rc = encode_3d(&mq, c.q, (uint64_t)c.d, (uint64_t)c.Sq, (uint64_t)c.B * c.Hq, 64, (uint32_t)p.g.Mq,
+                       (uint32_t)p.g.Gp, msg, msg_len);
+    if (rc == MERCURY_OK)
+        rc = encode_3d(&mk, c.k, (uint64_t)c.d, (uint64_t)c.Skv, (uint64_t)c.B * c.Hkv, 64, kTileKeys, 1, msg,
+                       msg_len);
+    if (rc == MERCURY_OK)
+        rc = encode_3d(&mv, c.v, (uint64_t)c.d, (uint64_t)c.Skv, (uint64_t)c.B * c.Hkv, 64, kTileKeys, 1, msg,
+                       msg_len);
+    if (rc == MERCURY_OK) {
+        if (c.d == 128)
+            rc = launch_impl<128, 2, 2>(p, mq, mk, mv, stream, msg, msg_len);
+        else
+            rc = launch_impl<64, 4, 4>(p, mq, mk, mv, stream, msg, msg_len);
+    }
+    return rc;
+}
+
+int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,
+                                size_t msg_len)
+{
+    unsigned int zero = 0, w = 0, s = 0;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(&w, g_err_word, sizeof w);
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(&s, g_err_site, sizeof s);
+    if (e == cudaSuccess && (w || s)) {
+        e = cudaMemcpyToSymbol(g_err_word, &zero, sizeof zero);
+        if (e == cudaSuccess)
+            e = cudaMemcpyToSymbol(g_err_site, &zero, sizeof zero);
+    }
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "reading the device error word: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    *word = w;
+    *site = s;
+    return MERCURY_OK;
+}
+
+}  // namespace mercury

@@ -1,0 +1,29 @@
+// internal.h -- declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/mercury_attn.h"
+
+namespace mercury {
+
+// One attention call, validated by the C-ABI layer.
+struct AttnCall {
+    const void *q, *k, *v;
+    int B, Hq, Hkv, Sq, Skv, d, R, causal, partial;
+    const int *order;  // [R*R] shift table from the planner
+    float *out, *lse;  // fused: out/lse; partial: o_part/lse_part
+    unsigned long long wait_ns;
+    int fault;
+};
+
+int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len);
+
+int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
+                     float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len);
+
+// Synchronise `stream`, read and clear the kernels' device error word.
+int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,
+                                size_t msg_len);
+
+}  // namespace mercury

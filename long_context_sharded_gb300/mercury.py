@@ -1,0 +1,197 @@
+"""Thin ctypes binding of libmercury_attn.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only turns torch tensors into pointers and sizes and status codes into
+exceptions.  It loads the in-tree library built by ``build.py`` and raises
+immediately if it is missing: there is no CPU fallback.
+
+The functions keep the C names:
+  mercury_plan_shift(R, shift)                      -> [R, R] int32 numpy table
+  mercury_attn_sharded(q, k, v, R, shift, causal, out=None, lse=None, stream=None)
+  mercury_attn_partial(q, k, v, R, shift, causal, o_part=None, lse_part=None, stream=None)
+  mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None)
+  mercury_sync_status(stream=None)
+Tensors: q [B,Hq,Sq,d], k/v [B,Hkv,Skv,d] bf16 CUDA tensors, contiguous.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MERCURY_OK = 0
+MERCURY_EINVAL = -1
+MERCURY_EALIGN = -2
+MERCURY_ECUDA = -3
+MERCURY_ETIMEOUT = -4
+MERCURY_ENOMEM = -5
+MERCURY_MAX_R = 128
+
+_STATUS_NAMES = {
+    MERCURY_EINVAL: "EINVAL", MERCURY_EALIGN: "EALIGN", MERCURY_ECUDA: "ECUDA",
+    MERCURY_ETIMEOUT: "ETIMEOUT", MERCURY_ENOMEM: "ENOMEM",
+}
+
+# Every symbol include/mercury_attn.h declares.
+EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial",
+            "mercury_lse_merge", "mercury_sync_status", "mercury_last_error",
+            "mercury_work_decomposition", "mercury_work_item_rows")
+
+
+class MercuryError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s (%d): %s" % (_STATUS_NAMES.get(status, "?"), status, message))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            "libmercury_attn.so is not built (%s); run long_context_sharded_gb300.build.build() "
+            "or __graft_entry__.build() first" % path)
+    lib = ctypes.CDLL(path)
+    i32, i64, p = ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
+    attn_args = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32, p, p, p]
+    lib.mercury_plan_shift.argtypes = [i32, i32, p]
+    lib.mercury_attn_sharded.argtypes = attn_args
+    lib.mercury_attn_partial.argtypes = attn_args
+    lib.mercury_lse_merge.argtypes = [p, p, i32, i64, i32, p, p, p]
+    lib.mercury_sync_status.argtypes = [p]
+    lib.mercury_last_error.argtypes = []
+    lib.mercury_last_error.restype = ctypes.c_char_p
+    lib.mercury_work_decomposition.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, p]
+    lib.mercury_work_item_rows.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           i64, p, p, p]
+    for name in EXPORTED:
+        if name != "mercury_last_error":
+            getattr(lib, name).restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def _check(rc: int) -> None:
+    if rc != MERCURY_OK:
+        raise MercuryError(rc, lib.mercury_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev_ptr(t, dtype_name, what):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % what)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if str(t.dtype) != dtype_name:
+        raise TypeError("%s must be %s (got %s)" % (what, dtype_name, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    return t.data_ptr()
+
+
+def mercury_plan_shift(R: int, shift: int) -> np.ndarray:
+    out = np.zeros((R * R if R > 0 else 1,), dtype=np.int32)
+    _check(lib.mercury_plan_shift(R, shift, out.ctypes.data_as(ctypes.c_void_p)))
+    return out.reshape(R, R)
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, S, d]")
+    B, Hq, Sq, d = q.shape
+    Bk, Hkv, Skv, dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or dk != d:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape),
+                                                             tuple(v.shape)))
+    return B, Hq, Hkv, Sq, Skv, d
+
+
+def mercury_attn_sharded(q, k, v, R: int, shift: int, causal: bool, out=None, lse=None,
+                         stream=None):
+    """Attention through the shifted schedule; returns (out fp32, lse fp32)."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    rc = lib.mercury_attn_sharded(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+        _dev_ptr(out, "torch.float32", "out"), _dev_ptr(lse, "torch.float32", "lse"),
+        _stream_ptr(stream))
+    _check(rc)
+    return out, lse
+
+
+def mercury_attn_partial(q, k, v, R: int, shift: int, causal: bool, o_part=None, lse_part=None,
+                         stream=None):
+    """Per-step partials; returns (o_part [R,B,Hq,Sq,d], lse_part [R,B,Hq,Sq])."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    if o_part is None:
+        o_part = torch.empty((R, B, Hq, Sq, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((R, B, Hq, Sq), dtype=torch.float32, device=q.device)
+    rc = lib.mercury_attn_partial(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+        _dev_ptr(o_part, "torch.float32", "o_part"), _dev_ptr(lse_part, "torch.float32", "lse_part"),
+        _stream_ptr(stream))
+    _check(rc)
+    return o_part, lse_part
+
+
+def mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None):
+    """Merge partials o_part [n, ..., d] / lse_part [n, ...] over the first axis."""
+    import torch
+    n_parts = o_part.shape[0]
+    d = o_part.shape[-1]
+    rows = o_part[0].numel() // d if n_parts else 0
+    if lse_part.shape[0] != n_parts or lse_part[0].numel() != rows:
+        raise ValueError("lse_part does not match o_part")
+    if out is None:
+        out = torch.empty(tuple(o_part.shape[1:]), dtype=torch.float32, device=o_part.device)
+    if lse is None:
+        lse = torch.empty(tuple(lse_part.shape[1:]), dtype=torch.float32, device=o_part.device)
+    rc = lib.mercury_lse_merge(
+        _dev_ptr(o_part, "torch.float32", "o_part"), _dev_ptr(lse_part, "torch.float32", "lse_part"),
+        n_parts, rows, d, _dev_ptr(out, "torch.float32", "out"),
+        _dev_ptr(lse, "torch.float32", "lse"), _stream_ptr(stream))
+    _check(rc)
+    return out, lse
+
+
+def mercury_sync_status(stream=None) -> None:
+    _check(lib.mercury_sync_status(_stream_ptr(stream)))
+
+
+def mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, partial):
+    info = (ctypes.c_longlong * 8)()
+    _check(lib.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, int(bool(causal)),
+                                          int(bool(partial)), info))
+    keys = ("Mq", "Gp", "head_mode", "T_h", "T_r", "items_per_group", "n_items")
+    return {k: int(info[i]) for i, k in enumerate(keys)}
+
+
+def mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, partial, item):
+    rows = (ctypes.c_longlong * 256)()
+    n = ctypes.c_int(0)
+    step = ctypes.c_int(0)
+    _check(lib.mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+                                      int(bool(partial)), item, rows, ctypes.byref(n),
+                                      ctypes.byref(step)))
+    return [rows[i] for i in range(n.value)], step.value

@@ -1,0 +1,276 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation, P rounded to bf16 before P.V):
+  O:   max |gpu - oracle| <= 2e-2 and mean |gpu - oracle| <= 2e-3
+  LSE: max |gpu - oracle| <= 1e-3
+Small shapes are compared on every row; the full-size workloads on a seeded
+row sample (block edges, the diagonal, random rows), plus a full-coverage
+cross-check of the fused path against partials + merge on the GPU.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_sharded_gb300.inputs import make_qkv, sample_rows
+from long_context_sharded_gb300.workloads import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_sharded_gb300 import build
+    build.build()
+    from long_context_sharded_gb300 import mercury
+    return mercury
+
+
+def assert_close(o_gpu, l_gpu, o_ref, l_ref, what=""):
+    o_gpu = np.asarray(o_gpu, dtype=np.float64).reshape(o_ref.shape)
+    l_gpu = np.asarray(l_gpu, dtype=np.float64).reshape(l_ref.shape)
+    assert np.isfinite(o_gpu).all(), what + ": non-finite O"
+    fin = np.isfinite(l_ref)
+    assert (np.isfinite(l_gpu) == fin).all(), what + ": LSE finiteness differs"
+    err = np.abs(o_gpu - o_ref)
+    lerr = np.abs(l_gpu[fin] - l_ref[fin]) if fin.any() else np.zeros(1)
+    msg = "%s: O max %.3g mean %.3g, LSE max %.3g" % (what, err.max(), err.mean(), lerr.max())
+    assert err.max() <= O_MAX, msg
+    assert err.mean() <= O_MEAN, msg
+    assert lerr.max() <= LSE_MAX, msg
+
+
+def run_sharded(m, q, k, v, R, shift, causal):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out, lse = m.mercury_attn_sharded(qd, kd, vd, R, shift, causal)
+    m.mercury_sync_status()
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def run_partial_merge(m, q, k, v, R, shift, causal):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    op, lp = m.mercury_attn_partial(qd, kd, vd, R, shift, causal)
+    out, lse = m.mercury_lse_merge(op, lp)
+    m.mercury_sync_status()
+    return op.cpu().numpy(), lp.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
+
+
+# ------------------------------------------------ structured probes (S vs PV)
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_probe_q_zero_mean_of_v(m, d):
+    """Q = 0: every score is 0, so O is the mean of V -- exercises P.V alone."""
+    _, k, v = make_qkv(1, 1, 1, 256, 256, d, seed=101)
+    q = torch.zeros(1, 1, 256, d, dtype=torch.bfloat16)
+    out, lse = run_sharded(m, q, k, v, 1, 1, False)
+    vv = v.to(torch.float64).numpy()[0, 0]
+    np.testing.assert_allclose(out[0, 0], np.broadcast_to(vv.mean(0), (256, d)), atol=2e-3)
+    np.testing.assert_allclose(lse[0, 0], math.log(256), atol=1e-4)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_probe_one_hot_selects_row(m, d):
+    """Dominant one-hot scores: query i and key j share coordinate (index mod d),
+    so row i attends (almost) only to keys j = i mod d -- exercises Q.K^T."""
+    S = 256
+    alpha = 16.0 if d == 64 else 24.0
+    q = torch.zeros(1, 1, S, d)
+    k = torch.zeros(1, 1, S, d)
+    idx = torch.arange(S)
+    q[0, 0, idx, idx % d] = alpha
+    k[0, 0, idx, (idx * 3) % d] = alpha
+    _, _, v = make_qkv(1, 1, 1, S, S, d, seed=5)
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    out, lse = run_sharded(m, q, k, v, 1, 1, False)
+    o_ref, l_ref = oracle.attn(q, k, v, False)
+    assert_close(out, lse, o_ref, l_ref, "one-hot")
+
+
+# ------------------------------------------------------ small shapes, all rows
+
+SMALL = [
+    # B, Hq, Hkv, Sq, Skv, d, R, shift, causal
+    (1, 4, 4, 512, 512, 64, 4, 1, False),      # the small MHA workload
+    (1, 1, 1, 128, 128, 128, 1, 1, False),     # one tile
+    (1, 2, 1, 256, 256, 128, 2, 1, True),      # GQA pair, causal diagonal
+    (2, 4, 2, 384, 384, 128, 3, 1, True),      # odd R, causal
+    (1, 8, 2, 512, 512, 64, 4, 0, True),       # unshifted order
+    (1, 8, 8, 1024, 1024, 128, 8, 4, True),    # nested 2x4 shift, MHA row pairs
+    (1, 8, 1, 128, 4096, 128, 4, 1, False),    # MQA, heads packed 4 per tile (Bq = 32)
+    (1, 8, 2, 96, 96, 64, 3, 1, True),         # Bq = 32, G = 4 packed, causal
+    (1, 3, 1, 200, 200, 128, 2, 1, True),      # ragged block and shard, odd group
+    (2, 2, 2, 384, 384, 64, 3, 1, False),      # MHA odd tile count
+    (1, 6, 3, 64, 192, 128, 8, 2, True),       # Bq = 8, Sq < Skv causal, nested
+    (1, 4, 1, 16, 16, 128, 1, 1, True),        # tiny
+    (1, 2, 2, 1000, 1000, 128, 1, 1, True),    # Skv not a multiple of 128
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_sharded_small_all_rows(m, cfg):
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]))
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(out, lse, o_ref, l_ref, "sharded")
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: "x".join(map(str, c)))
+def test_partial_small_all_rows(m, cfg):
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 1)
+    op, lp, out, lse = run_partial_merge(m, q, k, v, R, shift, causal)
+    op_ref, lp_ref = oracle.attn_partial(q, k, v, R, shift, causal)
+    assert_close(op, lp, op_ref, lp_ref, "partials")
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(out, lse, o_ref, l_ref, "partial+merge")
+
+
+def test_shift_orders_agree_on_gpu(m):
+    q, k, v = make_qkv(1, 4, 2, 1024, 1024, 128, seed=42)
+    o_ref, l_ref = oracle.attn(q, k, v, True)
+    for shift in (0, 1, 2, 4, 8):
+        out, lse = run_sharded(m, q, k, v, 8, shift, True)
+        assert_close(out, lse, o_ref, l_ref, "shift %d" % shift)
+
+
+def test_deterministic_replay(m):
+    q, k, v = make_qkv(1, 8, 2, 2048, 2048, 128, seed=9)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = m.mercury_attn_sharded(qd, kd, vd, 4, 1, True)
+    o2, l2 = m.mercury_attn_sharded(qd, kd, vd, 4, 1, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_output_canaries_untouched(m):
+    B, Hq, Hkv, S, d, R = 1, 4, 2, 320, 128, 2
+    q, k, v = make_qkv(B, Hq, Hkv, S, S, d, seed=3)
+    n_o, n_l = B * Hq * S * d, B * Hq * S
+    big_o = torch.full((n_o + 4096,), 7.25, device="cuda")
+    big_l = torch.full((n_l + 4096,), 7.25, device="cuda")
+    out = big_o[:n_o].view(B, Hq, S, d)
+    lse = big_l[:n_l].view(B, Hq, S)
+    m.mercury_attn_sharded(q.cuda(), k.cuda(), v.cuda(), R, 1, True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert (big_o[n_o:] == 7.25).all() and (big_l[n_l:] == 7.25).all()
+
+
+# ------------------------------------------------------ merge kernel
+
+@pytest.mark.parametrize("n_parts,rows,d", [(1, 7, 128), (4, 33, 64), (64, 1000, 128),
+                                            (3, 5, 4), (130, 17, 256), (8, 64, 12)])
+def test_lse_merge_matches_oracle(m, n_parts, rows, d):
+    g = torch.Generator().manual_seed(n_parts * 1000 + rows)
+    o = torch.randn(n_parts, rows, d, generator=g)
+    l = torch.randn(n_parts, rows, generator=g) * 4
+    l[:, 0] = -math.inf                     # a row with no contribution at all
+    if n_parts > 1:
+        l[0, 1:] = -math.inf                # masked parts
+        o[0, 1:] = 0.0
+    out, lse = m.mercury_lse_merge(o.cuda(), l.cuda())
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.lse_merge(o.double().numpy(), l.double().numpy())
+    fin = np.isfinite(l_ref)
+    assert (np.isfinite(lse.cpu().numpy()) == fin).all()
+    np.testing.assert_allclose(out.cpu().numpy(), o_ref, atol=1e-5, rtol=1e-5)
+    np.testing.assert_allclose(lse.cpu().numpy()[fin], l_ref[fin], atol=1e-5, rtol=0)
+
+
+# ------------------------------------------------------ fault path (no GPU fault)
+
+def test_bounded_wait_times_out_cleanly(m, monkeypatch):
+    """A dropped arrive makes a device wait run out: the kernel records
+    ETIMEOUT and returns; the context stays usable for the next call."""
+    q, k, v = make_qkv(1, 2, 1, 512, 512, 128, seed=1)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    monkeypatch.setenv("MERCURY_FAULT", "drop_p_arrive")
+    monkeypatch.setenv("MERCURY_WAIT_NS", "20000000")
+    m.mercury_attn_sharded(qd, kd, vd, 2, 1, False)
+    with pytest.raises(m.MercuryError) as e:
+        m.mercury_sync_status()
+    assert e.value.status == m.MERCURY_ETIMEOUT
+    monkeypatch.delenv("MERCURY_FAULT")
+    monkeypatch.delenv("MERCURY_WAIT_NS")
+    out, lse = m.mercury_attn_sharded(qd, kd, vd, 2, 1, False)
+    m.mercury_sync_status()
+    o_ref, l_ref = oracle.attn(q, k, v, False)
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "after timeout")
+
+
+def test_sync_check_env_reports_timeout(m, monkeypatch):
+    q, k, v = make_qkv(1, 2, 1, 256, 256, 64, seed=2)
+    monkeypatch.setenv("MERCURY_FAULT", "drop_p_arrive")
+    monkeypatch.setenv("MERCURY_WAIT_NS", "20000000")
+    monkeypatch.setenv("MERCURY_SYNC_CHECK", "1")
+    with pytest.raises(m.MercuryError) as e:
+        m.mercury_attn_sharded(q.cuda(), k.cuda(), v.cuda(), 1, 1, False)
+    assert e.value.status == m.MERCURY_ETIMEOUT
+    monkeypatch.delenv("MERCURY_FAULT")
+    m.mercury_attn_sharded(q.cuda(), k.cuda(), v.cuda(), 1, 1, False)
+
+
+# ------------------------------------------------------ full-size workloads
+
+def _run_workload(m, name, check_cross=True):
+    w = WORKLOADS[name]
+    B, Hq, Hkv, Sq, Skv, d = w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"]
+    R, shift, causal = w["R"], w["shift"], w["causal"]
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=w["seed"], scale=w["scale"])
+    rows = sample_rows(B, Hq, Sq, R, seed=w["seed"], n_heads=8 if B * Hq > 8 else B * Hq)
+    o_ref, l_ref = oracle.attn(q, k, v, causal, rows=rows)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    del q, k, v
+    if w["mode"] == "partial":
+        op, lp = m.mercury_attn_partial(qd, kd, vd, R, shift, causal)
+        out, lse = m.mercury_lse_merge(op, lp)
+        del op, lp
+    else:
+        out, lse = m.mercury_attn_sharded(qd, kd, vd, R, shift, causal)
+    m.mercury_sync_status()
+    ridx = torch.as_tensor(rows, device="cuda")
+    o_s = out.view(-1, d)[ridx].cpu().numpy()
+    l_s = lse.view(-1)[ridx].cpu().numpy()
+    assert_close(o_s, l_s, o_ref, l_ref, name + " sampled rows")
+    if check_cross:
+        # every row: fused vs partial + merge on the GPU
+        if w["mode"] == "partial":
+            o2, l2 = m.mercury_attn_sharded(qd, kd, vd, R, shift, causal)
+        else:
+            op, lp = m.mercury_attn_partial(qd, kd, vd, R, shift, causal)
+            o2, l2 = m.mercury_lse_merge(op, lp)
+            del op, lp
+        m.mercury_sync_status()
+        diff = (o2 - out).abs()
+        assert diff.max().item() <= O_MAX and diff.mean().item() <= O_MEAN
+        assert (l2 - lse).abs().max().item() <= LSE_MAX
+    del out, lse, qd, kd, vd
+    torch.cuda.empty_cache()
+
+
+def test_workload_mha_b1_h4_d64_s512_r4(m):
+    _run_workload(m, "mha_b1_h4_d64_s512_r4")
+
+
+def test_workload_gqa_32k_causal(m):
+    _run_workload(m, "gqa_b1_hq32_hkv8_d128_s32k_causal_r8")
+
+
+def test_workload_mha_b16_4k(m):
+    _run_workload(m, "mha_b16_h32_d128_s4k_r8")
+
+
+def test_workload_mqa_2m_merge(m):
+    _run_workload(m, "mqa_b1_hq8_hkv1_d128_sq2k_skv2m_r64_merge")
+
+
+@pytest.mark.slow
+def test_workload_gqa_128k_causal_nested(m):
+    _run_workload(m, "gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4", check_cross=True)
