@@ -1,0 +1,78 @@
+"""Host logic of bench.py without a GPU: max-over-ranks timing and whole-job
+throughput across two gloo ranks (the replica path of --gpus N), clock-log
+parsing, and the reference arm's rank filter."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.init_dist(world, "gloo")
+    elapsed = [0.5, 2.0][rank]           # rank 1 is the slow one
+    mx = bench.max_over_ranks(elapsed, world)
+    bench.barrier(world)
+    value = bench.aggregate_value(1e12, 10, world, mx)
+    q.put((rank, mx, value))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_timing_and_aggregate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, mx, value in res:
+        assert mx == 2.0                              # both ranks see the slowest time
+        assert value == pytest.approx(1e12 * 10 * 2 / 2.0)
+
+
+def test_single_rank_identity():
+    assert bench.max_over_ranks(1.25, 1) == 1.25
+    assert bench.aggregate_value(2.0, 3, 1, 1.5) == pytest.approx(4.0)
+
+
+def test_clock_summary_parsing():
+    rows = [
+        ["2026/12/02 10:00:00.100", "0", "1965 MHz", "2070 MHz", "900.1 W", "0x0", "Not Active",
+         "Not Active", "Not Active", "Not Active"],
+        ["2026/12/02 10:00:00.200", "0", "1980 MHz", "2070 MHz", "1200.0 W", "0x4", "Not Active",
+         "Not Active", "Not Active", "Active"],
+        ["2026/12/02 10:00:09.000", "0", "500 MHz", "2070 MHz", "90.0 W", "0x0", "Active",
+         "Not Active", "Not Active", "Not Active"],   # outside the window
+    ]
+    import datetime
+    t0 = datetime.datetime(2026, 12, 2, 10, 0, 0).timestamp()
+    s = bench.ClockSampler.summarise(rows, t0, t0 + 1.0)
+    assert s["samples"] == 2 and s["sm_mhz"] == pytest.approx(1972.5)
+    assert s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_nonzero_rank_does_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.run_reference(bench_args())
+    assert capsys.readouterr().out == ""
+
+
+def bench_args():
+    import argparse
+    return argparse.Namespace(workload="mha_b1_h4_d64_s512_r4", steps=1, warmup=3)
