@@ -46,7 +46,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": None, "bytes_per_launch": None, "profile": None}
+ATTN_TRAFFIC = {"source_sha": "1317a74a6afabca4", "bytes_per_launch": 2437547520,
+                "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
 # ------------------------------------------------------------------ helpers
