@@ -76,7 +76,9 @@ struct Ctl {
 };
 
 // Bounded wait on an mbarrier phase.  false: timed out here or elsewhere.
-__device__ __noinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Ctl c, uint32_t site)
+// Inlined: a call shared by warps with different setmaxnreg budgets does
+// not register-allocate.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Ctl c, uint32_t site)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -119,10 +121,20 @@ struct Smem {
     static constexpr int kOffV = kOffK + NK * kKVBytes;
     static constexpr int kOffBar = kOffV + NV * kKVBytes;
     static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 6;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;          // tmem slot, abort flag, n_total
+    static constexpr int kOffItem = kOffMisc + 16;                    // the decoded work item
+    static constexpr int kOffSteps = kOffItem + 64;                   // per step: key range lo, hi
+    static constexpr int kBytes = kOffSteps + 2 * 4 * kMaxR;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
+
+// Register split (setmaxnreg): the producer / MMA warpgroup gives registers
+// to the two softmax warpgroups.  The launch must provide at least
+// kMinLaunchRegs registers per thread (the host checks this before launching:
+// with fewer, setmaxnreg.inc would wait for registers that do not exist).
+constexpr uint32_t kRegsProducer = 56;
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr int kMinLaunchRegs = (int)((kRegsProducer + 2 * kRegsSoftmax) * 128 + kThreads - 1) / kThreads;
 
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -153,22 +165,32 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *o_full = p_full + 2;
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
+    int *n_total_s = (int *)(tmem_slot + 2);
+    int *step_lo = (int *)(smem + L::kOffSteps);
+    int *step_hi = step_lo + kMaxR;
 
+    Item *item_s = (Item *)(smem + L::kOffItem);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const Item it = decode_item(p.g, blockIdx.x);
-    const int ntile = it.t[1].valid ? 2 : 1;
+    const int nsteps = n_steps(p);
     const Ctl ctl{p.wait_ns, abort_flag};
 
-    // Total KV tiles of the item's shifted sequence.
-    int n_total = 0;
-    for (int st = 0; st < n_steps(p); ++st) {
-        int lo, hi;
-        shard_range(p.g, it, shard_at(p, it, st), lo, hi);
-        n_total += n_kv_tiles(lo, hi);
-    }
-
     if (threadIdx.x == 0) {
+        // Decode the work item once; the roles read it from shared memory so
+        // that little register state crosses into the register-split branches.
+        const Item it = decode_item(p.g, blockIdx.x);
+        *item_s = it;
+        // The item's shifted sequence: per step, the key range of its shard
+        // clipped to the causal limit (whole future shards become empty).
+        int total = 0;
+        for (int st = 0; st < nsteps; ++st) {
+            int lo, hi;
+            shard_range(p.g, it, shard_at(p, it, st), lo, hi);
+            step_lo[st] = lo;
+            step_hi[st] = hi;
+            total += n_kv_tiles(lo, hi);
+        }
+        *n_total_s = total;
         mbar_init(q_full, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(k_full + i, 1);
@@ -193,8 +215,16 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
+    // Each role sets its register budget inside its own branch and leaves
+    // through its own copy of the exit barrier, so no code runs under two
+    // budgets.  Warps 2-3 only give registers away.
+    if (warp < 4) {
+        regs_dec<kRegsProducer>();
+        const Item &it = *item_s;
+        const int ntile = it.t[1].valid ? 2 : 1;
+        const uint32_t tmem = *tmem_slot;
+        const int n_total = *n_total_s;
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0 && n_total > 0) {
@@ -209,10 +239,9 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             const int bkv = it.b * p.g.Hkv + it.hkv;
             int n = 0;
             bool ok = true;
-            for (int st = 0; st < n_steps(p) && ok; ++st) {
-                int lo, hi;
-                shard_range(p.g, it, shard_at(p, it, st), lo, hi);
-                const int nt = n_kv_tiles(lo, hi);
+            for (int st = 0; st < nsteps && ok; ++st) {
+                const int lo = step_lo[st];
+                const int nt = n_kv_tiles(lo, step_hi[st]);
                 for (int tt = 0; tt < nt; ++tt, ++n) {
                     const int k0 = lo + tt * kTileKeys;
                     const int sk = n % NK;
@@ -331,7 +360,19 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 }
             }
         }
-    } else if (warp >= 4) {
+    }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTmemCols);
+        }
+    } else {
+        regs_inc<kRegsSoftmax>();
+        const Item &it = *item_s;
+        const int ntile = it.t[1].valid ? 2 : 1;
+        const uint32_t tmem = *tmem_slot;
+        const int n_total = *n_total_s;
         // ------------------------------------------------------- softmax
         const int t = (warp - 4) / 4;
         const int quarter = warp % 4;  // tcgen05.ld lane quarter of this warp
@@ -341,92 +382,6 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             const int head = T.h0 + r / p.g.Mq;
             const int qi = T.q0 + r % p.g.Mq;
             const bool row_valid = (r % p.g.Mq) < T.nq;
-            const long long causal_lim =
-                p.g.causal ? (long long)qi + (p.g.Skv - p.g.Sq) : (long long)p.g.Skv;
-            const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
-            const uint32_t tS = tmem + lane_field + col_s(t);
-            const uint32_t tO = tmem + lane_field + col_o(t);
-            const float scale = p.scale_log2;
-            float m = -INFINITY;  // running max (log2 domain), possibly stale by < 2^8
-            float l = 0.f;        // running sum of 2^(y - m)
-            bool ok = true;
-            int n = 0;
-            for (int st = 0; st < n_steps(p) && ok; ++st) {
-                int lo, hi;
-                shard_range(p.g, it, shard_at(p, it, st), lo, hi);
-                const int nt = n_kv_tiles(lo, hi);
-                for (int tt = 0; tt < nt; ++tt, ++n) {
-                    const int k0 = lo + tt * kTileKeys;
-                    // allowed columns c: k0 + c < hi and k0 + c <= causal limit
-                    long long lim = (long long)hi - 1;
-                    if (causal_lim < lim)
-                        lim = causal_lim;
-                    lim -= k0;
-                    bool got = wait_phase(s_full + t, n & 1, ctl, 0x301);
-                    if (!__all_sync(0xffffffffu, got)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint32_t sr[128];
-                    tmem_ld_x128(tS, sr);
-                    float *s = reinterpret_cast<float *>(sr);
-                    if (lim < kTileKeys - 1) {
-#pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (c > lim)
-                                s[c] = -INFINITY;
-                    }
-                    float mx = s[0];
-#pragma unroll
-                    for (int c = 1; c < 128; ++c)
-                        mx = fmaxf(mx, s[c]);
-                    const float m_cand = fmaxf(m, mx * scale);
-                    const bool need = (m == -INFINITY) ? (m_cand != -INFINITY)
-                                                       : (m_cand - m > kRescaleThreshold);
-                    const float m_new = need ? m_cand : m;
-                    __syncwarp();
-                    if (n > 0 && __any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-                        l *= alpha;
-#pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t o[32];
-                            tmem_ld_x32(tO + c0, o);
-#pragma unroll
-                            for (int c = 0; c < 32; ++c)
-                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                            tmem_st_x32(tO + c0, o);
-                        }
-                    }
-                    m = m_new;
-                    const float mu = (m == -INFINITY) ? 0.f : m;
-                    float sum = 0.f;
-                    uint32_t pk[64];
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const float p0 = ex2_approx(fmaf(s[2 * c], scale, -mu));
-                        const float p1 = ex2_approx(fmaf(s[2 * c + 1], scale, -mu));
-                        sum += p0 + p1;
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);  // low half = p0
-                        pk[c] = *reinterpret_cast<uint32_t *>(&h2);
-                    }
-                    l += sum;
-                    uint32_t pa[32], pb[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        pa[c] = pk[c];
-                        pb[c] = pk[32 + c];
-                    }
-                    tmem_st_x32(tS, pa);
-                    tmem_st_x32(tS + 32, pb);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    if (!(p.fault == 1 && t == 0 && n == 0))
-                        mbar_arrive(p_full + t);
-                }
-            }
-            // ------------------------------------------------- epilogue
             float *orow = nullptr;
             float *lrow = nullptr;
             if (row_valid) {
@@ -440,6 +395,121 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 orow = p.out + so + row * D;
                 lrow = p.lse + sl + row;
             }
+            // last allowed key of this row (inclusive) under the causal mask
+            const int causal_lim = p.g.causal ? qi + (p.g.Skv - p.g.Sq) : 0x7fffffff;
+            const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
+            const uint32_t tS = tmem + lane_field + col_s(t);
+            const uint32_t tO = tmem + lane_field + col_o(t);
+            const float scale = p.scale_log2;
+            const uint64_t scale2 = f2_pack(scale, scale);
+            float m = -INFINITY;  // running max (log2 domain), possibly stale by < 2^8
+            float l = 0.f;        // running sum of 2^(y - m)
+            bool ok = true;
+            int n = 0;
+            for (int st = 0; st < nsteps && ok; ++st) {
+                const int lo = step_lo[st];
+                const int hi = step_hi[st];
+                const int nt = n_kv_tiles(lo, hi);
+                // allowed keys of this row in this step: k <= lim_abs
+                const int lim_abs = min(hi - 1, causal_lim);
+                for (int tt = 0; tt < nt; ++tt, ++n) {
+                    const int lim = lim_abs - (lo + tt * kTileKeys);  // allowed columns c <= lim
+                    bool got = wait_phase(s_full + t, n & 1, ctl, 0x301);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t sr[128];
+                    tmem_ld_x32x4(tS, sr);
+                    float *s = reinterpret_cast<float *>(sr);
+                    if (lim < kTileKeys - 1) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (c > lim)
+                                s[c] = -INFINITY;
+                    }
+                    // row max: four independent 3-input chains
+                    float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+                    float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+#pragma unroll
+                    for (int c = 8; c < 128; c += 8) {
+                        mx0 = max3f(mx0, s[c], s[c + 1]);
+                        mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+                        mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+                        mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+                    }
+                    const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
+                    const float m_cand = fmaxf(m, mx * scale);
+                    const bool need = (m == -INFINITY) ? (m_cand != -INFINITY)
+                                                       : (m_cand - m > kRescaleThreshold);
+                    const float m_new = need ? m_cand : m;
+                    __syncwarp();
+                    if (n > 0 && __any_sync(0xffffffffu, need)) {
+                        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+                        l *= alpha;
+                        const uint64_t alpha2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) {
+                                uint64_t v2 = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+                                                     alpha2);
+                                float a, b;
+                                f2_unpack(v2, a, b);
+                                o[c] = __float_as_uint(a);
+                                o[c + 1] = __float_as_uint(b);
+                            }
+                            tmem_st_x32(tO + c0, o);
+                        }
+                    }
+                    m = m_new;
+                    const float mu = (m == -INFINITY) ? 0.f : m;
+                    const uint64_t nmu2 = f2_pack(-mu, -mu);
+                    // p = 2^(s*scale - m): packed FMA, ex2 per element, packed
+                    // partial sums in four chains; bf16 pairs for the P.V MMA are
+                    // stored to tensor memory 16 columns (32 keys) at a time
+                    uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+#pragma unroll
+                    for (int cb = 0; cb < 64; cb += 16) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int c = 0; c < 16; c += 4) {
+                            uint64_t pp[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = 2 * (cb + c + u);
+                                const uint64_t x = f2_fma(f2_pack(s[e], s[e + 1]), scale2, nmu2);
+                                float x0, x1;
+                                f2_unpack(x, x0, x1);
+                                const float p0 = ex2_approx(x0);
+                                const float p1 = ex2_approx(x1);
+                                pp[u] = f2_pack(p0, p1);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);  // low half = p0
+                                pk[c + u] = *reinterpret_cast<uint32_t *>(&h2);
+                            }
+                            acc0 = f2_add(acc0, pp[0]);
+                            acc1 = f2_add(acc1, pp[1]);
+                            acc2 = f2_add(acc2, pp[2]);
+                            acc3 = f2_add(acc3, pp[3]);
+                        }
+                        tmem_st_x16(tS + cb, pk);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    if (!(p.fault == 1 && t == 0 && n == 0))
+                        mbar_arrive(p_full + t);
+                    float a0, a1, b0, b1, c0, c1, d0, d1;
+                    f2_unpack(acc0, a0, a1);
+                    f2_unpack(acc1, b0, b1);
+                    f2_unpack(acc2, c0, c1);
+                    f2_unpack(acc3, d0, d1);
+                    l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                }
+            }
+            // ------------------------------------------------- epilogue
             if (ok && n_total > 0) {
                 bool got = wait_phase(o_full + t, 0, ctl, 0x302);
                 ok = __all_sync(0xffffffffu, got);
@@ -471,13 +541,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 *lrow = -INFINITY;
             }
         }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tc_fence_before();
+        __syncthreads();
     }
 }
 
@@ -539,6 +604,22 @@ int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &m
             return MERCURY_ECUDA;
         }
         attr_set = true;
+    }
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) {
+            snprintf(msg, msg_len, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+            return MERCURY_ECUDA;
+        }
+        launch_regs = fa.numRegs;
+    }
+    // setmaxnreg.inc would wait for registers that the launch does not have
+    if (launch_regs < kMinLaunchRegs) {
+        snprintf(msg, msg_len, "kernel built with %d registers/thread, the register split needs %d",
+                 launch_regs, kMinLaunchRegs);
+        return MERCURY_ECUDA;
     }
     if (p.g.n_items > 0x7fffffffLL) {
         snprintf(msg, msg_len, "too many work items (%lld)", p.g.n_items);
