@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "1317a74a6afabca4", "bytes_per_launch": 2437547520,
+ATTN_TRAFFIC = {"source_sha": "4ff9735d3cf84af9", "bytes_per_launch": 2299224832,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
@@ -380,6 +380,16 @@ def measure_merge_path(m, dev, stream, peaks, peak_kind, reps: int = 10):
         torch.cuda.synchronize(dev)
         t_part.append(ev[0].elapsed_time(ev[1]) / 1e3)
         t_merge.append(ev[1].elapsed_time(ev[2]) / 1e3)
+    # the same chunk through mercury_attn_sharded: its schedule chooser cuts
+    # each rank's step sequence into runs and merges them (split-KV)
+    t_sh = []
+    for i in range(reps + 3):
+        ev[0].record(stream)
+        m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream)
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 3:
+            t_sh.append(ev[0].elapsed_time(ev[1]) / 1e3)
     m.mercury_sync_status(stream)
     rows = B * Hq * Sq
     merge_bytes = R * rows * (4 * d + 4) + rows * (4 * d + 4)
@@ -391,8 +401,10 @@ def measure_merge_path(m, dev, stream, peaks, peak_kind, reps: int = 10):
             "attention_frac": round(flops / tp / 1e12 / peaks["bf16_tflops"], 4),
             "merge_ms": round(tm * 1e3, 4), "merge_bytes": merge_bytes, "merge_gbs": round(gbs, 1),
             "merge_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-            "total_tflops": round(flops / (tp + tm) / 1e12, 2), "peak_kind": peak_kind,
-            "reps": reps}
+            "total_tflops": round(flops / (tp + tm) / 1e12, 2),
+            "sharded_auto_ms": round(statistics.median(t_sh) * 1e3, 4),
+            "sharded_auto_tflops": round(flops / statistics.median(t_sh) / 1e12, 2),
+            "peak_kind": peak_kind, "reps": reps}
 
 
 # --------------------------------------------------------- reference arm

@@ -91,6 +91,14 @@ MERCURY_API int mercury_plan_shift(int R, int shift, int *order);
  * (mercury_plan_shift(R, shift)); under causal masking a shard entirely in the
  * future of a block is skipped and the diagonal shard is masked per element.
  * Writes out [B,Hq,Sq,d] fp32 and lse [B,Hq,Sq] fp32.
+ * Schedule: when one work item per rank's whole step sequence would leave the
+ * GPU short of work (short query side, long KV), each rank's step sequence is
+ * cut into g runs of consecutive steps; each run's partial (O, LSE) goes to
+ * scratch memory and the runs are merged as by mercury_lse_merge.  The
+ * scratch, g * B*Hq*Sq*(d+1)*4 bytes (at most 4 GiB, env
+ * MERCURY_SCRATCH_MAX_BYTES), comes stream-ordered from a memory pool the
+ * library keeps per device; env MERCURY_SPLIT_GROUPS=g forces g runs (1: no
+ * split).  The result is the same up to rounding.
  * Requirements: B, Hq, Hkv, Sq, Skv >= 1; Hq % Hkv == 0; d in {64, 128};
  * 1 <= R <= MERCURY_MAX_R; Sq % R == 0 and Skv % R == 0; causal requires
  * Sq <= Skv; valid shift (as in mercury_plan_shift); every element count fits
@@ -159,20 +167,24 @@ MERCURY_API const char *mercury_last_error(void);
  * (Gp), pairing mode (1: the two tiles of a work item are two head groups at
  * the same rows; 0: two consecutive row tiles of the same heads), head tiles
  * per KV group, row tiles per query block, work items per (batch, KV head,
- * rank), total work items, 0.  partial selects mercury_attn_partial's split.
+ * rank), total work items, output slots.  mode: 0 the fused schedule of
+ * mercury_attn_sharded, 1 mercury_attn_partial's per-step split, g >= 2 the
+ * split into g runs of steps (g is rounded so every run but the last has
+ * ceil(R/g) steps).
  * Errors: MERCURY_EINVAL for arguments a compute call would reject.
  */
 MERCURY_API int mercury_work_decomposition(int B, int Hq, int Hkv, int Sq, int Skv, int d,
-                               int R, int causal, int partial, long long *info);
+                               int R, int causal, int mode, long long *info);
 
 /*
  * mercury_work_item_rows -- for work item `item` of that decomposition, writes
- * the flat rows ((b*Hq + h)*Sq + q) it computes and the step it writes
- * (partial) or -1 (sharded): rows[0..n-1], *n_rows = n (at most 256), *step.
- * Pure host code, for coverage tests.  Errors: MERCURY_EINVAL.
+ * the flat rows ((b*Hq + h)*Sq + q) it computes and the output slot it writes
+ * (mode 1: the step; mode >= 2: the run) or -1 (mode 0): rows[0..n-1],
+ * *n_rows = n (at most 256), *step.  Pure host code, for coverage tests.
+ * Errors: MERCURY_EINVAL.
  */
 MERCURY_API int mercury_work_item_rows(int B, int Hq, int Hkv, int Sq, int Skv, int d,
-                           int R, int shift, int causal, int partial,
+                           int R, int shift, int causal, int mode,
                            long long item, long long *rows, int *n_rows, int *step);
 
 #ifdef __cplusplus

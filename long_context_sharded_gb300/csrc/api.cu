@@ -134,6 +134,115 @@ int finish(int rc, cudaStream_t stream)
     return ok();
 }
 
+// Number of SMs of the current device (cached per device).
+int sm_count(int *out)
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return MERCURY_OK;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64)
+        cache[dev] = n;
+    *out = n;
+    return MERCURY_OK;
+}
+
+long long env_ll(const char *name, long long dflt)
+{
+    const char *e = getenv(name);
+    if (!e || !*e)
+        return dflt;
+    char *end = nullptr;
+    long long v = strtoll(e, &end, 10);
+    return (end && *end == '\0') ? v : dflt;
+}
+
+// Schedule chooser for mercury_attn_sharded: the fused schedule (one work
+// item per rank's whole step sequence) unless it leaves the GPU short of
+// work, in which case each rank's shifted step sequence is cut into runs
+// whose partials are merged afterwards -- the latency / memory trade the
+// pages describe (Silicon & Systems, "Memory capacity is part of
+// performance"): more runs fill the SMs but cost scratch and merge traffic.
+// A small cost model picks the run count: waves of work items x run length,
+// plus a per-item set-up cost, plus the merge's HBM traffic; scratch is
+// capped at MERCURY_SCRATCH_MAX_BYTES (default 4 GiB).  Returns the number of
+// runs (1 = fused).  MERCURY_SPLIT_GROUPS forces it.
+int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int causal, int sms)
+{
+    long long forced = env_ll("MERCURY_SPLIT_GROUPS", 0);
+    if (forced >= 1)
+        return (int)(forced < R ? forced : R);
+    Geom g;
+    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, kFused) || sms < 1)
+        return 1;
+    if (R == 1 || g.n_items >= 4LL * sms)
+        return 1;  // enough items: the fused schedule keeps every SM busy
+    const double t_tile = 1.3e-6;   // one 128-key tile through a two-tile item
+    const double t_item = 4e-6;     // per item: set-up, Q load, epilogue
+    const double merge_bw = 6e12;   // bytes per second of the merge
+    const long long cap = env_ll("MERCURY_SCRATCH_MAX_BYTES", 4LL << 30);
+    const double per_slot = (double)B * Hq * Sq * (d + 1) * 4;
+    const double tiles_per_step = (double)((g.Bk + kTileKeys - 1) / kTileKeys);
+    double best = 0;
+    int best_g = 1;
+    for (int gr = 1; gr <= R; ++gr) {
+        const int spg = (R + gr - 1) / gr;
+        if ((R + spg - 1) / spg != gr)
+            continue;  // same runs as a smaller count
+        if (gr > 1 && gr * per_slot > (double)cap)
+            break;
+        const long long items = g.n_items * gr;
+        const long long waves = (items + sms - 1) / sms;
+        double cost = waves * (spg * tiles_per_step * t_tile + t_item);
+        if (gr > 1)
+            cost += (gr + 1) * per_slot / merge_bw;
+        if (gr == 1 || cost < best) {
+            best = cost;
+            best_g = gr;
+        }
+    }
+    return best_g;
+}
+
+// Library-private stream-ordered pool for split-KV scratch (per device;
+// memory is kept for reuse instead of being returned at every synchronise).
+int scratch_pool(cudaMemPool_t *pool)
+{
+    static cudaMemPool_t pools[64] = {};
+    static bool made[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64)
+        return fail(MERCURY_ECUDA, "device ordinal %d out of range", dev);
+    if (!made[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        e = cudaMemPoolCreate(&pools[dev], &props);
+        if (e != cudaSuccess)
+            return fail(MERCURY_ECUDA, "cudaMemPoolCreate: %s", cudaGetErrorString(e));
+        unsigned long long keep = ~0ull;
+        e = cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess)
+            return fail(MERCURY_ECUDA, "cudaMemPoolSetAttribute: %s", cudaGetErrorString(e));
+        made[dev] = true;
+    }
+    *pool = pools[dev];
+    return MERCURY_OK;
+}
+
 int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                 int d, int R, int shift, int causal, float *out, float *lse, void *stream, int partial)
 {
@@ -143,6 +252,15 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     int order[kMaxR * kMaxR];
     if (plan_shift(R, shift, order))
         return fail(MERCURY_EINVAL, "invalid (R, shift)");
+    cudaStream_t s = (cudaStream_t)stream;
+    int groups = 1;
+    if (!partial) {
+        int sms = 0;
+        rc = sm_count(&sms);
+        if (rc)
+            return rc;
+        groups = choose_groups(B, Hq, Hkv, Sq, Skv, d, R, causal, sms);
+    }
     AttnCall c;
     c.q = q;
     c.k = k;
@@ -155,14 +273,42 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     c.d = d;
     c.R = R;
     c.causal = causal ? 1 : 0;
-    c.partial = partial;
+    c.mode = partial ? kPerStep : (groups > 1 ? kGrouped : kFused);
+    c.n_groups = partial ? R : groups;
     c.order = order;
     c.out = out;
     c.lse = lse;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
-    cudaStream_t s = (cudaStream_t)stream;
+    if (c.mode != kGrouped) {
+        rc = launch_attention(c, s, g_msg, sizeof g_msg);
+        return finish(rc, s);
+    }
+    // split-KV: partials of every run into pooled scratch, then the merge
+    Geom g;
+    make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, kGrouped, groups);
+    const long long rows = (long long)B * Hq * Sq;
+    const size_t o_bytes = (size_t)g.n_groups * rows * d * sizeof(float);
+    const size_t l_bytes = (size_t)g.n_groups * rows * sizeof(float);
+    cudaMemPool_t pool;
+    rc = scratch_pool(&pool);
+    if (rc)
+        return rc;
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes, pool, s);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "split-KV scratch (%zu bytes): %s", o_bytes + l_bytes,
+                    cudaGetErrorString(e));
+    float *o_part = (float *)scratch;
+    float *l_part = (float *)((char *)scratch + o_bytes);
+    c.out = o_part;
+    c.lse = l_part;
     rc = launch_attention(c, s, g_msg, sizeof g_msg);
+    if (rc == MERCURY_OK)
+        rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, d, out, lse, s, g_msg, sizeof g_msg);
+    e = cudaFreeAsync(scratch, s);
+    if (rc == MERCURY_OK && e != cudaSuccess)
+        rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
     return finish(rc, s);
 }
 
@@ -242,8 +388,11 @@ int mercury_work_decomposition(int B, int Hq, int Hkv, int Sq, int Skv, int d, i
         return fail(MERCURY_EINVAL, "head dim must be 64 or 128 (got %d)", d);
     if (causal && Sq > Skv)
         return fail(MERCURY_EINVAL, "causal attention needs Sq <= Skv");
+    if (partial < 0)
+        return fail(MERCURY_EINVAL, "mode must be >= 0");
     Geom g;
-    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, partial))
+    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, partial >= 2 ? kGrouped : partial,
+                  partial >= 2 ? partial : 1))
         return fail(MERCURY_EINVAL, "unsupported shape");
     info[0] = g.Mq;
     info[1] = g.Gp;
@@ -252,7 +401,7 @@ int mercury_work_decomposition(int B, int Hq, int Hkv, int Sq, int Skv, int d, i
     info[4] = g.T_r;
     info[5] = (long long)g.NHP * g.NRT;
     info[6] = g.n_items;
-    info[7] = 0;
+    info[7] = g.n_groups;
     return ok();
 }
 
@@ -269,7 +418,8 @@ int mercury_work_item_rows(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R
     if (rc)
         return rc;
     Geom g;
-    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, partial))
+    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, partial >= 2 ? kGrouped : partial,
+                  partial >= 2 ? partial : 1))
         return fail(MERCURY_EINVAL, "unsupported shape");
     if (item < 0 || item >= g.n_items)
         return fail(MERCURY_EINVAL, "item out of range");
@@ -290,10 +440,12 @@ int mercury_work_item_rows(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R
     }
     *n_rows = n;
     *step = -1;
-    if (partial) {
+    if (g.partial == kPerStep) {
         for (int j = 0; j < R; ++j)
             if (order[it.rank * R + j] == it.shard)
                 *step = j;
+    } else if (g.partial == kGrouped) {
+        *step = it.shard;
     }
     return ok();
 }

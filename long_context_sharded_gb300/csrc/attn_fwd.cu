@@ -58,8 +58,8 @@ struct AttnParams {
     long long slot_o;        // partial: elements between slots of o_part
     long long slot_lse;      // partial: elements between slots of lse_part
     unsigned long long wait_ns;
-    // fused: tab[i*R + j] = shard of rank i at step j;
-    // partial: tab[i*R + s] = step (slot) at which rank i reads shard s.
+    // fused, grouped: tab[i*R + j] = shard of rank i at step j;
+    // per step: tab[i*R + s] = step (slot) at which rank i reads shard s.
     unsigned char tab[kMaxR * kMaxR];
 };
 
@@ -99,16 +99,20 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Ctl c
     }
 }
 
-// Shard visited at step `step` of the item's sequence (fused: R steps;
-// partial: one step, the item's shard).
+// Shard visited at step `step` of the item's sequence (fused: the rank's R
+// steps; per step: the item's shard; grouped: the item's run of steps).
 __device__ __forceinline__ int shard_at(const AttnParams &p, const Item &it, int step)
 {
-    return p.g.partial ? it.shard : (int)p.tab[it.rank * p.g.R + step];
+    if (p.g.partial == kPerStep)
+        return it.shard;
+    const int j = p.g.partial == kGrouped ? it.shard * p.g.spg + step : step;
+    return (int)p.tab[it.rank * p.g.R + j];
 }
 
-__device__ __forceinline__ int n_steps(const AttnParams &p)
+// Output slot of a non-fused item: the step (per step) or the run (grouped).
+__device__ __forceinline__ int out_slot(const AttnParams &p, const Item &it)
 {
-    return p.g.partial ? 1 : p.g.R;
+    return p.g.partial == kPerStep ? (int)p.tab[it.rank * p.g.R + it.shard] : it.shard;
 }
 
 template <int D, int NK, int NV>
@@ -172,7 +176,6 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     Item *item_s = (Item *)(smem + L::kOffItem);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    const int nsteps = n_steps(p);
     const Ctl ctl{p.wait_ns, abort_flag};
 
     if (threadIdx.x == 0) {
@@ -180,6 +183,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         // that little register state crosses into the register-split branches.
         const Item it = decode_item(p.g, blockIdx.x);
         *item_s = it;
+        const int nsteps = item_steps(p.g, it);
+        n_total_s[1] = nsteps;
         // The item's shifted sequence: per step, the key range of its shard
         // clipped to the causal limit (whole future shards become empty).
         int total = 0;
@@ -190,7 +195,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             step_hi[st] = hi;
             total += n_kv_tiles(lo, hi);
         }
-        *n_total_s = total;
+        n_total_s[0] = total;
         mbar_init(q_full, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(k_full + i, 1);
@@ -224,7 +229,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         const Item &it = *item_s;
         const int ntile = it.t[1].valid ? 2 : 1;
         const uint32_t tmem = *tmem_slot;
-        const int n_total = *n_total_s;
+        const int n_total = n_total_s[0];
+        const int nsteps = n_total_s[1];
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0 && n_total > 0) {
@@ -372,7 +378,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         const Item &it = *item_s;
         const int ntile = it.t[1].valid ? 2 : 1;
         const uint32_t tmem = *tmem_slot;
-        const int n_total = *n_total_s;
+        const int n_total = n_total_s[0];
+        const int nsteps = n_total_s[1];
         // ------------------------------------------------------- softmax
         const int t = (warp - 4) / 4;
         const int quarter = warp % 4;  // tcgen05.ld lane quarter of this warp
@@ -387,8 +394,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             if (row_valid) {
                 long long row = ((long long)it.b * p.g.Hq + head) * p.g.Sq + qi;
                 long long so = 0, sl = 0;
-                if (p.g.partial) {
-                    const int slot = p.tab[it.rank * p.g.R + it.shard];
+                if (p.g.partial != kFused) {
+                    const int slot = out_slot(p, it);
                     so = slot * p.slot_o;
                     sl = slot * p.slot_lse;
                 }
@@ -642,7 +649,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     // storage: the launch path makes no heap allocation.
     static thread_local AttnParams p;
     memset(&p, 0, sizeof p);
-    if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.partial)) {
+    if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups)) {
         snprintf(msg, msg_len, "unsupported shape");
         return MERCURY_EINVAL;
     }
@@ -657,7 +664,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     for (int i = 0; i < R; ++i)
         for (int j = 0; j < R; ++j) {
             const int s = c.order[i * R + j];
-            if (c.partial)
+            if (c.mode == kPerStep)
                 p.tab[i * R + s] = (unsigned char)j;
             else
                 p.tab[i * R + j] = (unsigned char)s;

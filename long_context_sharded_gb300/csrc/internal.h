@@ -10,9 +10,11 @@ namespace mercury {
 // One attention call, validated by the C-ABI layer.
 struct AttnCall {
     const void *q, *k, *v;
-    int B, Hq, Hkv, Sq, Skv, d, R, causal, partial;
+    int B, Hq, Hkv, Sq, Skv, d, R, causal;
+    int mode;          // kFused, kPerStep or kGrouped (work.h)
+    int n_groups;      // kGrouped: runs of steps per rank
     const int *order;  // [R*R] shift table from the planner
-    float *out, *lse;  // fused: out/lse; partial: o_part/lse_part
+    float *out, *lse;  // fused: out/lse; otherwise [slots][B,Hq,Sq,(d)] partials
     unsigned long long wait_ns;
     int fault;
 };

@@ -28,8 +28,17 @@ constexpr int kMaxR = 128;      // largest R (shift table fits the kernel parame
 constexpr int kTileRows = 128;  // M of the tcgen05 MMA: query rows per tile
 constexpr int kTileKeys = 128;  // keys per K/V tile: N of S = Q K^T, K of O += P V
 
+// Modes of a call: kFused runs all R steps of a rank in one work item (one
+// output); kPerStep gives every (rank, shard) pair its own item and output
+// slot (the step at which the rank reads that shard); kGrouped splits each
+// rank's step sequence into n_groups runs of consecutive steps, one output
+// slot per run, merged afterwards (split-KV for short query sides).
+enum Mode { kFused = 0, kPerStep = 1, kGrouped = 2 };
+
 struct Geom {
-    int B, Hq, Hkv, Sq, Skv, d, R, causal, partial;
+    int B, Hq, Hkv, Sq, Skv, d, R, causal, partial;  // partial: mode (Mode)
+    int n_groups;   // kGrouped: runs per rank; else 1 (fused) or R (per step)
+    int spg;        // steps per run (kGrouped), R (fused), 1 (per step)
     int G;          // query heads per KV head
     int Bq, Bk;     // rows per query block / keys per KV shard
     int Mq, Gp;     // queries per head in a tile, heads per tile (Mq*Gp = 128)
@@ -40,17 +49,33 @@ struct Geom {
     long long n_items;
 };
 
-// Choose the tile geometry.  Returns 0, or -1 when the shape is unsupported.
+// Choose the tile geometry.  mode: kFused, kPerStep or kGrouped (then
+// n_groups in [1, R] runs; the run length is ceil(R / n_groups) steps and the
+// run count is recomputed from it).  Returns 0, or -1 when unsupported.
 inline int make_geom(Geom &g, int B, int Hq, int Hkv, int Sq, int Skv, int d, int R,
-                     int causal, int partial)
+                     int causal, int mode, int n_groups = 1)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || R < 1 || R > kMaxR)
         return -1;
     if (Hq % Hkv != 0 || Sq % R != 0 || Skv % R != 0)
         return -1;
+    if (mode != kFused && mode != kPerStep && mode != kGrouped)
+        return -1;
+    if (mode == kGrouped && (n_groups < 1 || n_groups > R))
+        return -1;
     g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.Sq = Sq; g.Skv = Skv; g.d = d; g.R = R;
     g.causal = causal ? 1 : 0;
-    g.partial = partial ? 1 : 0;
+    g.partial = mode;
+    if (mode == kFused) {
+        g.spg = R;
+        g.n_groups = 1;
+    } else if (mode == kPerStep) {
+        g.spg = 1;
+        g.n_groups = R;
+    } else {
+        g.spg = (R + n_groups - 1) / n_groups;
+        g.n_groups = (R + g.spg - 1) / g.spg;
+    }
     g.G = Hq / Hkv;
     g.Bq = Sq / R;
     g.Bk = Skv / R;
@@ -66,7 +91,7 @@ inline int make_geom(Geom &g, int B, int Hq, int Hkv, int Sq, int Skv, int d, in
     g.NHP = g.head_mode ? (g.T_h + 1) / 2 : 1;
     g.NRT = g.head_mode ? g.T_r : (g.T_r + 1) / 2;
     long long per_rank = (long long)g.NHP * g.Hkv * g.B * g.NRT;
-    g.n_items = per_rank * R * (g.partial ? R : 1);
+    g.n_items = per_rank * R * (g.partial == kFused ? 1 : g.n_groups);
     return 0;
 }
 
@@ -79,7 +104,7 @@ struct Tile {
 
 struct Item {
     int b, hkv, rank;
-    int shard;  // partial mode: the KV shard; fused: -1
+    int shard;  // kPerStep: the KV shard; kGrouped: the run index; fused: -1
     Tile t[2];
     int kv_end; // keys [0, kv_end) can be attended by some row of the item
 };
@@ -87,8 +112,9 @@ struct Item {
 // Decode work item `idx`.  Fused causal items are ordered heaviest first
 // (longest KV range first) so that a wave of CTAs ends together; items that
 // share a KV head sit next to each other so concurrent CTAs share K/V in L2.
-// Partial items are ordered by shard first, so CTAs resident together read
-// the same shard.
+// Per-step items are ordered by shard first, so CTAs resident together read
+// the same shard; grouped items by run first (neighbouring ranks' runs
+// overlap in shards under the shift).
 MERCURY_HD Item decode_item(const Geom &g, long long idx)
 {
     Item it;
@@ -97,8 +123,8 @@ MERCURY_HD Item decode_item(const Geom &g, long long idx)
     it.b = (int)(idx % g.B); idx /= g.B;
     int rt = (int)(idx % g.NRT); idx /= g.NRT;
     int rank = (int)(idx % g.R); idx /= g.R;
-    it.shard = g.partial ? (int)idx : -1;
-    if (g.causal && !g.partial) {
+    it.shard = g.partial != kFused ? (int)idx : -1;
+    if (g.causal && g.partial == kFused) {
         rank = g.R - 1 - rank;
         rt = g.NRT - 1 - rt;
     }
@@ -141,6 +167,18 @@ MERCURY_HD void shard_range(const Geom &g, const Item &it, int s, int &lo, int &
     hi = lo + g.Bk;
     if (hi > it.kv_end)
         hi = it.kv_end;
+}
+
+// Steps in the item's sequence: all R (fused), one (per step), or the
+// item's run of consecutive steps (grouped).
+MERCURY_HD int item_steps(const Geom &g, const Item &it)
+{
+    if (g.partial == kFused)
+        return g.R;
+    if (g.partial == kPerStep)
+        return 1;
+    const int rest = g.R - it.shard * g.spg;
+    return rest < g.spg ? rest : g.spg;
 }
 
 MERCURY_HD int n_kv_tiles(int lo, int hi)

@@ -179,19 +179,20 @@ def mercury_sync_status(stream=None) -> None:
     _check(lib.mercury_sync_status(_stream_ptr(stream)))
 
 
-def mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, partial):
+def mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, mode):
+    """mode: 0 fused, 1 per-step partials, g >= 2 split into g runs of steps."""
     info = (ctypes.c_longlong * 8)()
     _check(lib.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, int(bool(causal)),
-                                          int(bool(partial)), info))
-    keys = ("Mq", "Gp", "head_mode", "T_h", "T_r", "items_per_group", "n_items")
+                                          int(mode), info))
+    keys = ("Mq", "Gp", "head_mode", "T_h", "T_r", "items_per_group", "n_items", "slots")
     return {k: int(info[i]) for i, k in enumerate(keys)}
 
 
-def mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, partial, item):
+def mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, mode, item):
     rows = (ctypes.c_longlong * 256)()
     n = ctypes.c_int(0)
     step = ctypes.c_int(0)
     _check(lib.mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
-                                      int(bool(partial)), item, rows, ctypes.byref(n),
+                                      int(mode), item, rows, ctypes.byref(n),
                                       ctypes.byref(step)))
     return [rows[i] for i in range(n.value)], step.value

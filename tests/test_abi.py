@@ -126,7 +126,7 @@ def test_workload_geometry(m, name):
     from long_context_sharded_gb300.workloads import WORKLOADS
     w = WORKLOADS[name]
     info = m.mercury_work_decomposition(w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"],
-                                        w["R"], w["causal"], w["mode"] == "partial")
+                                        w["R"], w["causal"], 1 if w["mode"] == "partial" else 0)
     assert (info["Mq"], info["Gp"], info["head_mode"]) == WORKLOAD_GEOMS[name]
     assert info["n_items"] < 2 ** 31
 
@@ -144,24 +144,35 @@ COVERAGE = [
 
 
 @pytest.mark.parametrize("cfg", COVERAGE)
-@pytest.mark.parametrize("partial", [False, True])
-def test_work_items_cover_each_output_once(m, cfg, partial):
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 5])
+def test_work_items_cover_each_output_once(m, cfg, mode):
     B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
-    info = m.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, partial)
+    if mode > R:
+        pytest.skip("more runs than steps")
+    info = m.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, mode)
+    slots = info["slots"]
+    if mode == 0:
+        assert slots == 1
+    elif mode == 1:
+        assert slots == R
+    else:
+        spg = -(-R // mode)
+        assert slots == -(-R // spg) and slots <= mode
     seen = {}
     for item in range(info["n_items"]):
-        rows, step = m.mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, partial, item)
+        rows, step = m.mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, mode, item)
         assert len(rows) <= 256
-        if partial:
-            assert 0 <= step < R
+        if mode:
+            assert 0 <= step < slots
         else:
             assert step == -1
         for r in rows:
             key = (r, step)
-            assert key not in seen, "row %d step %d written twice" % key
+            assert key not in seen, "row %d slot %d written twice" % key
             seen[key] = item
-    expect = B * Hq * Sq * (R if partial else 1)
+    expect = B * Hq * Sq * (slots if mode else 1)
     assert len(seen) == expect
+    partial = mode == 1
     if partial:
         # the item writing (row, step j) reads shard order[rank][j]
         order = m.mercury_plan_shift(R, shift)

@@ -133,6 +133,33 @@ def test_partial_small_all_rows(m, cfg):
     assert_close(out, lse, o_ref, l_ref, "partial+merge")
 
 
+@pytest.mark.parametrize("groups", [1, 2, 3, 8])
+@pytest.mark.parametrize("cfg", [(1, 8, 1, 128, 4096, 128, 8, 1, False),
+                                 (1, 4, 2, 512, 1024, 64, 8, 4, True),
+                                 (2, 2, 2, 384, 384, 128, 3, 1, True)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_sharded_split_runs_match_oracle(m, monkeypatch, cfg, groups):
+    """mercury_attn_sharded with the shifted step sequence cut into runs
+    (split-KV through library scratch + merge) equals plain attention."""
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", str(groups))
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + groups)
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(out, lse, o_ref, l_ref, "split into %d runs" % groups)
+
+
+def test_sharded_auto_split_on_long_kv(m):
+    """A short query side over a long KV: the chooser splits (the GPU would
+    otherwise hold 16 work items for its SMs); result equals plain attention."""
+    info = m.mercury_work_decomposition(1, 8, 1, 512, 65536, 128, 16, False, 0)
+    assert info["n_items"] < 8 * torch.cuda.get_device_properties(0).multi_processor_count
+    q, k, v = make_qkv(1, 8, 1, 512, 65536, 128, seed=77)
+    out, lse = run_sharded(m, q, k, v, 16, 1, False)
+    o_ref, l_ref = oracle.attn(q, k, v, False)
+    assert_close(out, lse, o_ref, l_ref, "auto split")
+
+
 def test_shift_orders_agree_on_gpu(m):
     q, k, v = make_qkv(1, 4, 2, 1024, 1024, 128, seed=42)
     o_ref, l_ref = oracle.attn(q, k, v, True)
