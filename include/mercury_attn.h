@@ -149,6 +149,37 @@ MERCURY_API int mercury_lse_merge(const float *o_part, const float *lse_part, in
                       long long rows, int d, float *out, float *lse, void *stream);
 
 /*
+ * mercury_attn_split_noalloc -- mercury_attn_sharded's split-KV schedule for
+ * callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * Callers inside an allocator or memory manager, serving or real-time loops
+ * that forbid allocator calls on their hot path, and hosts that give the
+ * library a fixed device-memory budget cannot let a call allocate scratch.
+ * This call cuts each rank's shifted step sequence into n_runs runs (as
+ * mercury_attn_sharded does when it splits), keeps the runs' partial (O, LSE)
+ * in a fixed 64 MiB array that the library's module holds on every GPU that
+ * loads it (until the process exits), and merges them into out / lse.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments as mercury_attn_sharded, plus 1 <= n_runs <= R (rounded like the
+ * run count of mercury_work_decomposition).  The partials need
+ * runs * B*Hq*Sq*(d+1)*4 bytes; more than 64 MiB is rejected with
+ * MERCURY_EINVAL before any work.
+ * The first call on a device looks up the array's device address with that
+ * device current; make it before any stream capture.  All calls on a device
+ * share the array: calls that can overlap on the GPU (other streams, other
+ * threads) race and corrupt each other's results.  The array keeps the last
+ * call's contents; nothing in it needs to start at zero, since each call
+ * writes every partial it reads.
+ * Errors: MERCURY_EINVAL, MERCURY_EALIGN, MERCURY_ECUDA, and
+ * MERCURY_ETIMEOUT when MERCURY_SYNC_CHECK=1.
+ */
+MERCURY_API int mercury_attn_split_noalloc(const void *q, const void *k, const void *v,
+                               int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                               int R, int shift, int causal, int n_runs,
+                               float *out, float *lse, void *stream);
+
+/*
  * mercury_sync_status -- synchronise `stream`, then read and clear the device
  * error word of this process's kernels.  Returns MERCURY_OK,
  * MERCURY_ETIMEOUT (a bounded device wait ran out in some earlier kernel) or

@@ -363,6 +363,16 @@ int mercury_lse_merge(const float *o_part, const float *lse_part, int n_parts, l
     return finish(rc, s);
 }
 
+int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq,
+                               int Skv, int d, int R, int shift, int causal, int n_runs, float *out,
+                               float *lse, void *stream)
+{
+    cudaStream_t s = (cudaStream_t)stream;
+    int rc = attn_split_noalloc(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_runs, out, lse, s,
+                                g_msg, sizeof g_msg);
+    return finish(rc, s);
+}
+
 int mercury_sync_status(void *stream)
 {
     unsigned int w = 0, site = 0;

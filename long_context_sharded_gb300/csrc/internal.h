@@ -24,6 +24,12 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
 int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
                      float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len);
 
+// The split-KV schedule with its partials in the library's fixed-size
+// device array instead of allocated scratch (noalloc.cu).
+int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
+                       int d, int R, int shift, int causal, int n_runs, float *out, float *lse,
+                       cudaStream_t stream, char *msg, size_t msg_len);
+
 // Synchronise `stream`, read and clear the kernels' device error word.
 int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,
                                 size_t msg_len);

@@ -38,7 +38,7 @@ _STATUS_NAMES = {
 # Every symbol include/mercury_attn.h declares.
 EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial",
             "mercury_lse_merge", "mercury_sync_status", "mercury_last_error",
-            "mercury_work_decomposition", "mercury_work_item_rows")
+            "mercury_work_decomposition", "mercury_work_item_rows", "mercury_attn_split_noalloc")
 
 
 class MercuryError(RuntimeError):
@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.mercury_attn_sharded.argtypes = attn_args
     lib.mercury_attn_partial.argtypes = attn_args
     lib.mercury_lse_merge.argtypes = [p, p, i32, i64, i32, p, p, p]
+    lib.mercury_attn_split_noalloc.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                               i32, p, p, p]
     lib.mercury_sync_status.argtypes = [p]
     lib.mercury_last_error.argtypes = []
     lib.mercury_last_error.restype = ctypes.c_char_p
@@ -171,6 +173,21 @@ def mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None):
         _dev_ptr(o_part, "torch.float32", "o_part"), _dev_ptr(lse_part, "torch.float32", "lse_part"),
         n_parts, rows, d, _dev_ptr(out, "torch.float32", "out"),
         _dev_ptr(lse, "torch.float32", "lse"), _stream_ptr(stream))
+    _check(rc)
+    return out, lse
+
+
+def mercury_attn_split_noalloc(q, k, v, R: int, shift: int, causal: bool, n_runs: int, out, lse,
+                               stream=None):
+    """Split-KV attention whose partials live in the library's fixed 64 MiB
+    device array: no device memory is allocated (out and lse are the
+    caller's).  Calls that may overlap on the GPU must not share a device."""
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    rc = lib.mercury_attn_split_noalloc(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+        int(n_runs), _dev_ptr(out, "torch.float32", "out"), _dev_ptr(lse, "torch.float32", "lse"),
+        _stream_ptr(stream))
     _check(rc)
     return out, lse
 
