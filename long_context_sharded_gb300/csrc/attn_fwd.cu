@@ -124,7 +124,8 @@ struct Smem {
     static constexpr int kOffK = 2 * kQBytes;
     static constexpr int kOffV = kOffK + NK * kKVBytes;
     static constexpr int kOffBar = kOffV + NV * kKVBytes;
-    static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 6;
+    static constexpr int NE = NK > NV ? NK : NV;  // ring of "stage free" events
+    static constexpr int kNumBars = 1 + NK + NV + NE + 6;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;          // tmem slot, abort flag, n_total
     static constexpr int kOffItem = kOffMisc + 16;                    // the decoded work item
     static constexpr int kOffSteps = kOffItem + 64;                   // per step: key range lo, hi
@@ -161,10 +162,13 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *bars = (uint64_t *)(smem + L::kOffBar);
     uint64_t *q_full = bars;
     uint64_t *k_full = q_full + 1;
-    uint64_t *k_empty = k_full + NK;
-    uint64_t *v_full = k_empty + NK;
-    uint64_t *v_empty = v_full + NV;
-    uint64_t *s_full = v_empty + NV;
+    uint64_t *v_full = k_full + NK;
+    // kv_free[n % NE], phase n / NE: S of the last tile at tile-iteration n is
+    // done, so K(n) and V(n-1) are no longer read.  Forwarded by a softmax
+    // thread that waits on s_full anyway: a tcgen05.commit costs the MMA
+    // issuer about as much as an MMA, so the issuer commits only s_full/o_full.
+    uint64_t *kv_free = v_full + NV;
+    uint64_t *s_full = kv_free + L::NE;
     uint64_t *p_full = s_full + 2;
     uint64_t *o_full = p_full + 2;
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
@@ -197,14 +201,12 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         }
         n_total_s[0] = total;
         mbar_init(q_full, 1);
-        for (int i = 0; i < NK; ++i) {
+        for (int i = 0; i < NK; ++i)
             mbar_init(k_full + i, 1);
-            mbar_init(k_empty + i, 1);
-        }
-        for (int i = 0; i < NV; ++i) {
+        for (int i = 0; i < NV; ++i)
             mbar_init(v_full + i, 1);
-            mbar_init(v_empty + i, 1);
-        }
+        for (int i = 0; i < L::NE; ++i)
+            mbar_init(kv_free + i, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full + t, 1);
             mbar_init(p_full + t, 128);
@@ -251,7 +253,9 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 for (int tt = 0; tt < nt; ++tt, ++n) {
                     const int k0 = lo + tt * kTileKeys;
                     const int sk = n % NK;
-                    if (n >= NK && !wait_phase(k_empty + sk, ((n / NK) - 1) & 1, ctl, 0x101)) {
+                    // stage sk held K(n - NK): free once iteration n - NK is done
+                    const int ek = n - NK;
+                    if (ek >= 0 && !wait_phase(kv_free + ek % L::NE, (ek / L::NE) & 1, ctl, 0x101)) {
                         ok = false;
                         break;
                     }
@@ -260,7 +264,9 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk,
                                     c * 64, k0, bkv);
                     const int sv = n % NV;
-                    if (n >= NV && !wait_phase(v_empty + sv, ((n / NV) - 1) & 1, ctl, 0x102)) {
+                    // stage sv held V(n - NV): free once iteration n - NV + 1 is done
+                    const int ev = n - NV + 1;
+                    if (n >= NV && !wait_phase(kv_free + ev % L::NE, (ev / L::NE) & 1, ctl, 0x102)) {
                         ok = false;
                         break;
                     }
@@ -330,14 +336,12 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     }
                     if (!ok)
                         break;
-                    umma_commit(v_empty + sv);
                 } else {
                     for (int t = 0; t < ntile; ++t) {
                         issue_qk(t, sk);
                         umma_commit(s_full + t);
                     }
                 }
-                umma_commit(k_empty + sk);
             }
             if (ok) {
                 const int last = n_total - 1;
@@ -354,15 +358,6 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     tc_fence_after();
                     issue_pv(t, sv, last > 0);
                     umma_commit(o_full + t);
-                }
-                if (ok) {
-                    umma_commit(v_empty + sv);
-                    // Drain: let the last release of every ring stage land before
-                    // the CTA's shared memory goes away.
-                    for (int m = (n_total > NK ? n_total - NK : 0); m < n_total && ok; ++m)
-                        ok = wait_phase(k_empty + (m % NK), (m / NK) & 1, ctl, 0x207);
-                    for (int m = (n_total > NV ? n_total - NV : 0); m < n_total && ok; ++m)
-                        ok = wait_phase(v_empty + (m % NV), (m / NV) & 1, ctl, 0x208);
                 }
             }
         }
@@ -427,6 +422,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         break;
                     }
                     tc_fence_after();
+                    if (t == ntile - 1 && r == 0)
+                        mbar_arrive(kv_free + n % L::NE);  // K(n), V(n-1) free
                     uint32_t sr[128];
                     tmem_ld_x32x4(tS, sr);
                     float *s = reinterpret_cast<float *>(sr);
