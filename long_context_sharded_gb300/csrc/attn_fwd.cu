@@ -124,12 +124,10 @@ struct Smem {
     static constexpr int kOffK = 2 * kQBytes;
     static constexpr int kOffV = kOffK + NK * kKVBytes;
     static constexpr int kOffBar = kOffV + NV * kKVBytes;
-    static constexpr int NE = NK > NV ? NK : NV;  // ring of "stage free" events
-    static constexpr int kNumBars = 1 + NK + NV + NE + 6;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;          // tmem slot, abort flag, n_total
-    static constexpr int kOffItem = kOffMisc + 16;                    // the decoded work item
-    static constexpr int kOffSteps = kOffItem + 64;                   // per step: key range lo, hi
-    static constexpr int kBytes = kOffSteps + 2 * 4 * kMaxR;
+    static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
+    static constexpr int kNumBars = 1 + NK + NV + NE + 8;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem slot, abort flag
+    static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -137,16 +135,40 @@ struct Smem {
 // to the two softmax warpgroups.  The launch must provide at least
 // kMinLaunchRegs registers per thread (the host checks this before launching:
 // with fewer, setmaxnreg.inc would wait for registers that do not exist).
-constexpr uint32_t kRegsProducer = 56;
-constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsProducer = 104;
+constexpr uint32_t kRegsSoftmax = 200;
 constexpr int kMinLaunchRegs = (int)((kRegsProducer + 2 * kRegsSoftmax) * 128 + kThreads - 1) / kThreads;
 
+// Key range [lo, hi) of step st of an item; returns its number of KV tiles.
+__device__ __forceinline__ int step_range(const AttnParams &p, const Item &it, int st, int &lo, int &hi)
+{
+    shard_range(p.g, it, shard_at(p, it, st), lo, hi);
+    return n_kv_tiles(lo, hi);
+}
+
+// KV tiles of the item's whole shifted sequence.
+__device__ __forceinline__ int item_tiles(const AttnParams &p, const Item &it)
+{
+    int n = 0;
+    const int ns = item_steps(p.g, it);
+    for (int st = 0; st < ns; ++st) {
+        int lo, hi;
+        n += step_range(p, it, st, lo, hi);
+    }
+    return n;
+}
+
+// Persistent: each CTA (one per SM) takes work items blockIdx.x,
+// blockIdx.x + gridDim.x, ...  (heaviest first for causal calls).  Barrier
+// phases run on across items; the MMA issuer starts the next item's Q K^T
+// while the softmax warps still write out the previous item's O.
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
 {
     using L = Smem<D, NK, NV>;
+    constexpr int NE = L::NE;
     constexpr int NBOX = D / 64;  // 128-byte swizzle columns per row
     // tensor-memory columns of S_t and O_t
     auto col_s = [](int t) { return (uint32_t)(t * 128); };
@@ -163,54 +185,38 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *q_full = bars;
     uint64_t *k_full = q_full + 1;
     uint64_t *v_full = k_full + NK;
-    // kv_free[n % NE], phase n / NE: S of the last tile at tile-iteration n is
-    // done, so K(n) and V(n-1) are no longer read.  Forwarded by a softmax
-    // thread that waits on s_full anyway: a tcgen05.commit costs the MMA
-    // issuer about as much as an MMA, so the issuer commits only s_full/o_full.
+    // kv_free[g % NE], phase g / NE: the CTA's tile-iteration g (counted across
+    // its items) is done -- S of the item's last tile is computed, so K(g) and
+    // V(g-1) are no longer read, nor Q once g is an item's last iteration.
+    // A softmax thread that waits on s_full anyway forwards it: a
+    // tcgen05.commit costs the MMA issuer about as much as an MMA, so the
+    // issuer commits only s_full and o_full.
     uint64_t *kv_free = v_full + NV;
-    uint64_t *s_full = kv_free + L::NE;
+    uint64_t *s_full = kv_free + NE;
     uint64_t *p_full = s_full + 2;
     uint64_t *o_full = p_full + 2;
+    uint64_t *o_free = o_full + 2;  // O_t read out by the softmax warps
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
-    int *n_total_s = (int *)(tmem_slot + 2);
-    int *step_lo = (int *)(smem + L::kOffSteps);
-    int *step_hi = step_lo + kMaxR;
 
-    Item *item_s = (Item *)(smem + L::kOffItem);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const Ctl ctl{p.wait_ns, abort_flag};
+    const long long n_items = p.g.n_items;
 
     if (threadIdx.x == 0) {
-        // Decode the work item once; the roles read it from shared memory so
-        // that little register state crosses into the register-split branches.
-        const Item it = decode_item(p.g, blockIdx.x);
-        *item_s = it;
-        const int nsteps = item_steps(p.g, it);
-        n_total_s[1] = nsteps;
-        // The item's shifted sequence: per step, the key range of its shard
-        // clipped to the causal limit (whole future shards become empty).
-        int total = 0;
-        for (int st = 0; st < nsteps; ++st) {
-            int lo, hi;
-            shard_range(p.g, it, shard_at(p, it, st), lo, hi);
-            step_lo[st] = lo;
-            step_hi[st] = hi;
-            total += n_kv_tiles(lo, hi);
-        }
-        n_total_s[0] = total;
         mbar_init(q_full, 1);
         for (int i = 0; i < NK; ++i)
             mbar_init(k_full + i, 1);
         for (int i = 0; i < NV; ++i)
             mbar_init(v_full + i, 1);
-        for (int i = 0; i < L::NE; ++i)
+        for (int i = 0; i < NE; ++i)
             mbar_init(kv_free + i, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full + t, 1);
             mbar_init(p_full + t, 128);
             mbar_init(o_full + t, 1);
+            mbar_init(o_free + t, 4);  // one arrive per softmax warp
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -228,71 +234,79 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     // budgets.  Warps 2-3 only give registers away.
     if (warp < 4) {
         regs_dec<kRegsProducer>();
-        const Item &it = *item_s;
-        const int ntile = it.t[1].valid ? 2 : 1;
         const uint32_t tmem = *tmem_slot;
-        const int n_total = n_total_s[0];
-        const int nsteps = n_total_s[1];
-    if (warp == 0) {
-        // ------------------------------------------------------- TMA producer
-        if (lane == 0 && n_total > 0) {
+        if (warp == 0 && lane == 0) {
+            // --------------------------------------------------- TMA producer
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQBytes));
-            for (int t = 0; t < ntile; ++t)
-                for (int c = 0; c < NBOX; ++c)
-                    tma_load_3d(sQ + t * L::kQBytes + c * L::kBoxBytes, &tmQ, q_full, c * 64,
-                                it.t[t].q0, it.b * p.g.Hq + it.t[t].h0);
-            const int bkv = it.b * p.g.Hkv + it.hkv;
-            int n = 0;
+            int g = 0;  // tile-iterations issued so far by this CTA
             bool ok = true;
-            for (int st = 0; st < nsteps && ok; ++st) {
-                const int lo = step_lo[st];
-                const int nt = n_kv_tiles(lo, step_hi[st]);
-                for (int tt = 0; tt < nt; ++tt, ++n) {
-                    const int k0 = lo + tt * kTileKeys;
-                    const int sk = n % NK;
-                    // stage sk held K(n - NK): free once iteration n - NK is done
-                    const int ek = n - NK;
-                    if (ek >= 0 && !wait_phase(kv_free + ek % L::NE, (ek / L::NE) & 1, ctl, 0x101)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(k_full + sk, (uint32_t)L::kKVBytes);
+            for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const Item it = decode_item(p.g, idx);
+                const int ntot = item_tiles(p, it);
+                if (ntot == 0)
+                    continue;
+                const int ntile = it.t[1].valid ? 2 : 1;
+                // the Q buffer is free once the previous item's last iteration is done
+                if (g > 0 && !wait_phase(kv_free + (g - 1) % NE, ((g - 1) / NE) & 1, ctl, 0x103)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQBytes));
+                for (int t = 0; t < ntile; ++t)
                     for (int c = 0; c < NBOX; ++c)
-                        tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk,
-                                    c * 64, k0, bkv);
-                    const int sv = n % NV;
-                    // stage sv held V(n - NV): free once iteration n - NV + 1 is done
-                    const int ev = n - NV + 1;
-                    if (n >= NV && !wait_phase(kv_free + ev % L::NE, (ev / L::NE) & 1, ctl, 0x102)) {
-                        ok = false;
-                        break;
+                        tma_load_3d(sQ + t * L::kQBytes + c * L::kBoxBytes, &tmQ, q_full, c * 64,
+                                    it.t[t].q0, it.b * p.g.Hq + it.t[t].h0);
+                const int bkv = it.b * p.g.Hkv + it.hkv;
+                const int nsteps = item_steps(p.g, it);
+                for (int st = 0; st < nsteps && ok; ++st) {
+                    int lo, hi;
+                    const int nt = step_range(p, it, st, lo, hi);
+                    for (int tt = 0; tt < nt; ++tt, ++g) {
+                        const int k0 = lo + tt * kTileKeys;
+                        // stage g % NK held K(g - NK): free once iteration g - NK is done
+                        const int ek = g - NK;
+                        if (ek >= 0 && !wait_phase(kv_free + ek % NE, (ek / NE) & 1, ctl, 0x101)) {
+                            ok = false;
+                            break;
+                        }
+                        const int sk = g % NK;
+                        mbar_arrive_expect_tx(k_full + sk, (uint32_t)L::kKVBytes);
+                        for (int c = 0; c < NBOX; ++c)
+                            tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk, c * 64,
+                                        k0, bkv);
+                        // stage g % NV held V(g - NV): free once iteration g - NV + 1 is done
+                        const int ev = g - NV + 1;
+                        if (g >= NV && !wait_phase(kv_free + ev % NE, (ev / NE) & 1, ctl, 0x102)) {
+                            ok = false;
+                            break;
+                        }
+                        const int sv = g % NV;
+                        mbar_arrive_expect_tx(v_full + sv, (uint32_t)L::kKVBytes);
+                        for (int c = 0; c < NBOX; ++c)
+                            tma_load_3d(sV + sv * L::kKVBytes + c * L::kBoxBytes, &tmV, v_full + sv, c * 64,
+                                        k0, bkv);
                     }
-                    mbar_arrive_expect_tx(v_full + sv, (uint32_t)L::kKVBytes);
-                    for (int c = 0; c < NBOX; ++c)
-                        tma_load_3d(sV + sv * L::kKVBytes + c * L::kBoxBytes, &tmV, v_full + sv,
-                                    c * 64, k0, bkv);
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && n_total > 0) {
-            const uint32_t q_base = smem_u32(sQ);
-            const uint32_t k_base = smem_u32(sK);
-            const uint32_t v_base = smem_u32(sV);
+        } else if (warp == 1 && lane == 0) {
+            // --------------------------------------------------- MMA issuer
+            // Descriptors: the address field (bits 0-13, bytes >> 4) of a base
+            // descriptor plus a constant offset never carries out of the field
+            // (shared memory < 256 KB), so stepping is one add.
+            const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv = smem_desc_sw128(smem_u32(sV), L::kBoxBytes, 1024);
             // S_t = Q_t K^T over K = D: 16 elements (32 bytes) per MMA inside a
             // 128-byte swizzle column; 8-row groups 1024 bytes apart.
             auto issue_qk = [&](int t, int sk) {
-                const uint32_t qa = q_base + t * L::kQBytes;
-                const uint32_t kb = k_base + sk * L::kKVBytes;
+                const uint64_t da = dq + ((uint32_t)(t * L::kQBytes) >> 4);
+                const uint64_t db = dk + ((uint32_t)(sk * L::kKVBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * L::kBoxBytes + (kk % 4) * 32;
-                    umma_ss(tmem + col_s(t), smem_desc_sw128(qa + off, 16, 1024),
-                            smem_desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
+                    umma_ss(tmem + col_s(t), da + off, db + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V over K = 128 keys: P_t from tensor memory (bf16 pairs,
@@ -300,68 +314,78 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             // two 8-row groups = 2048 bytes; the two 64-wide d halves are
             // kBoxBytes apart (leading-dimension offset).
             auto issue_pv = [&](int t, int sv, bool acc_in) {
-                const uint32_t vb = v_base + sv * L::kKVBytes;
+                const uint64_t db = dv + ((uint32_t)(sv * L::kKVBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                    umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
-                            smem_desc_sw128(vb + kk * 2048, L::kBoxBytes, 1024), kIdescPV,
-                            (acc_in || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kTileKeys / 16; ++kk)
+                    umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, db + (uint32_t)(kk * (2048 >> 4)),
+                            kIdescPV, (acc_in || kk > 0) ? 1u : 0u);
             };
-            bool ok = wait_phase(q_full, 0, ctl, 0x201);
-            tc_fence_after();
-            int n = 0;
-            for (; n < n_total && ok; ++n) {
-                const int sk = n % NK;
-                if (!wait_phase(k_full + sk, (n / NK) & 1, ctl, 0x202)) {
-                    ok = false;
-                    break;
-                }
+            int g = 0;                  // tile-iterations of this CTA so far
+            int nq = 0;                 // items with work so far (q_full phases)
+            int sp[2] = {0, 0};         // S_t / P_t phases so far, per tile
+            int od[2] = {0, 0};         // O_t finalisations so far, per tile
+            bool ok = true;
+            for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const Item it = decode_item(p.g, idx);
+                const int ntot = item_tiles(p, it);
+                if (ntot == 0)
+                    continue;
+                const int ntile = it.t[1].valid ? 2 : 1;
+                ok = wait_phase(q_full, nq & 1, ctl, 0x201);
+                ++nq;
                 tc_fence_after();
-                if (n > 0) {
-                    const int sv = (n - 1) % NV;
-                    for (int t = 0; t < ntile && ok; ++t) {
-                        if (!wait_phase(p_full + t, (n - 1) & 1, ctl, 0x203)) {
-                            ok = false;
-                            break;
-                        }
-                        if (t == 0 && !wait_phase(v_full + sv, ((n - 1) / NV) & 1, ctl, 0x204)) {
+                // iteration n issues P.V of n-1 (n >= 1) and Q K^T of n (n < ntot)
+                for (int n = 0; n <= ntot && ok; ++n) {
+                    const int sk = g % NK;
+                    if (n < ntot) {
+                        if (!wait_phase(k_full + sk, (g / NK) & 1, ctl, 0x202)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_pv(t, sv, n - 1 > 0);
-                        issue_qk(t, sk);
-                        umma_commit(s_full + t);
                     }
-                    if (!ok)
-                        break;
-                } else {
-                    for (int t = 0; t < ntile; ++t) {
-                        issue_qk(t, sk);
-                        umma_commit(s_full + t);
+                    if (n == 0) {
+                        for (int t = 0; t < ntile; ++t) {
+                            issue_qk(t, sk);
+                            umma_commit(s_full + t);
+                            ++sp[t];
+                        }
+                    } else {
+                        const int gv = g - 1;  // V of the previous iteration
+                        const int sv = gv % NV;
+                        if (!wait_phase(v_full + sv, (gv / NV) & 1, ctl, 0x204)) {
+                            ok = false;
+                            break;
+                        }
+                        for (int t = 0; t < ntile && ok; ++t) {
+                            if (!wait_phase(p_full + t, (sp[t] - 1) & 1, ctl, 0x203)) {
+                                ok = false;
+                                break;
+                            }
+                            // the item's first P.V overwrites O_t: the softmax warps
+                            // must have read out the previous item's O_t
+                            if (n == 1 && od[t] > 0 &&
+                                !wait_phase(o_free + t, (od[t] - 1) & 1, ctl, 0x205)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(t, sv, n > 1);
+                            if (n < ntot) {
+                                issue_qk(t, sk);
+                                umma_commit(s_full + t);
+                                ++sp[t];
+                            } else {
+                                umma_commit(o_full + t);
+                                ++od[t];
+                            }
+                        }
                     }
-                }
-            }
-            if (ok) {
-                const int last = n_total - 1;
-                const int sv = last % NV;
-                for (int t = 0; t < ntile && ok; ++t) {
-                    if (!wait_phase(p_full + t, last & 1, ctl, 0x205)) {
-                        ok = false;
-                        break;
-                    }
-                    if (t == 0 && !wait_phase(v_full + sv, (last / NV) & 1, ctl, 0x206)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(t, sv, last > 0);
-                    umma_commit(o_full + t);
+                    if (n < ntot)
+                        ++g;
                 }
             }
         }
-    }
         tc_fence_before();
         __syncthreads();
         if (warp == 1) {
@@ -370,16 +394,28 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         }
     } else {
         regs_inc<kRegsSoftmax>();
-        const Item &it = *item_s;
-        const int ntile = it.t[1].valid ? 2 : 1;
         const uint32_t tmem = *tmem_slot;
-        const int n_total = n_total_s[0];
-        const int nsteps = n_total_s[1];
         // ------------------------------------------------------- softmax
         const int t = (warp - 4) / 4;
         const int quarter = warp % 4;  // tcgen05.ld lane quarter of this warp
         const int r = quarter * 32 + lane;
-        if (t < ntile) {
+        const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_field + col_s(t);
+        const uint32_t tO = tmem + lane_field + col_o(t);
+        const float scale = p.scale_log2;
+        const uint64_t scale2 = f2_pack(scale, scale);
+        int g = 0;   // tile-iterations of this CTA so far (all tiles)
+        int sp = 0;  // S_t / P_t phases of this tile so far
+        int od = 0;  // O_t finalisations of this tile so far
+        bool ok = true;
+        for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            const Item it = decode_item(p.g, idx);
+            const int ntot = item_tiles(p, it);
+            const int ntile = it.t[1].valid ? 2 : 1;
+            if (t >= ntile) {
+                g += ntot;
+                continue;
+            }
             const Tile &T = it.t[t];
             const int head = T.h0 + r / p.g.Mq;
             const int qi = T.q0 + r % p.g.Mq;
@@ -397,33 +433,39 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 orow = p.out + so + row * D;
                 lrow = p.lse + sl + row;
             }
+            if (ntot == 0) {
+                // no allowed key for any row of this item in this shard
+                if (orow) {
+                    float4 *dst = reinterpret_cast<float4 *>(orow);
+                    for (int c = 0; c < D / 4; ++c)
+                        dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *lrow = -INFINITY;
+                }
+                continue;
+            }
             // last allowed key of this row (inclusive) under the causal mask
             const int causal_lim = p.g.causal ? qi + (p.g.Skv - p.g.Sq) : 0x7fffffff;
-            const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
-            const uint32_t tS = tmem + lane_field + col_s(t);
-            const uint32_t tO = tmem + lane_field + col_o(t);
-            const float scale = p.scale_log2;
-            const uint64_t scale2 = f2_pack(scale, scale);
+            const bool forwards = (t == ntile - 1) && r == 0;  // reports iteration done
             float m = -INFINITY;  // running max (log2 domain), possibly stale by < 2^8
             float l = 0.f;        // running sum of 2^(y - m)
-            bool ok = true;
             int n = 0;
+            const int nsteps = item_steps(p.g, it);
             for (int st = 0; st < nsteps && ok; ++st) {
-                const int lo = step_lo[st];
-                const int hi = step_hi[st];
-                const int nt = n_kv_tiles(lo, hi);
+                int lo, hi;
+                const int nt = step_range(p, it, st, lo, hi);
                 // allowed keys of this row in this step: k <= lim_abs
                 const int lim_abs = min(hi - 1, causal_lim);
                 for (int tt = 0; tt < nt; ++tt, ++n) {
                     const int lim = lim_abs - (lo + tt * kTileKeys);  // allowed columns c <= lim
-                    bool got = wait_phase(s_full + t, n & 1, ctl, 0x301);
+                    bool got = wait_phase(s_full + t, sp & 1, ctl, 0x301);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
+                    ++sp;
                     tc_fence_after();
-                    if (t == ntile - 1 && r == 0)
-                        mbar_arrive(kv_free + n % L::NE);  // K(n), V(n-1) free
+                    if (forwards)
+                        mbar_arrive(kv_free + (g + n) % NE);
                     uint32_t sr[128];
                     tmem_ld_x32x4(tS, sr);
                     float *s = reinterpret_cast<float *>(sr);
@@ -513,37 +555,37 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
                 }
             }
+            g += ntot;
+            if (!ok)
+                break;
             // ------------------------------------------------- epilogue
-            if (ok && n_total > 0) {
-                bool got = wait_phase(o_full + t, 0, ctl, 0x302);
-                ok = __all_sync(0xffffffffu, got);
-                if (ok) {
-                    tc_fence_after();
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
+            bool got = wait_phase(o_full + t, od & 1, ctl, 0x302);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok)
+                break;
+            ++od;
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld_x32(tO + c0, o);
-                        if (orow) {
-                            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(tO + c0, o);
+                if (orow) {
+                    float4 *dst = reinterpret_cast<float4 *>(orow + c0);
 #pragma unroll
-                            for (int c = 0; c < 8; ++c)
-                                dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv,
-                                                     __uint_as_float(o[4 * c + 1]) * inv,
-                                                     __uint_as_float(o[4 * c + 2]) * inv,
-                                                     __uint_as_float(o[4 * c + 3]) * inv);
-                        }
-                    }
-                    if (lrow)
-                        *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    for (int c = 0; c < 8; ++c)
+                        dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
+                                             __uint_as_float(o[4 * c + 2]) * inv,
+                                             __uint_as_float(o[4 * c + 3]) * inv);
                 }
-            } else if (n_total == 0 && orow) {
-                // no allowed key for any row of this item in this shard
-                float4 *dst = reinterpret_cast<float4 *>(orow);
-                for (int c = 0; c < D / 4; ++c)
-                    dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                *lrow = -INFINITY;
             }
+            // O_t is read: the next item's first P.V may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(o_free + t);
+            if (lrow)
+                *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
         tc_fence_before();
         __syncthreads();
@@ -629,7 +671,23 @@ int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &m
         snprintf(msg, msg_len, "too many work items (%lld)", p.g.n_items);
         return MERCURY_EINVAL;
     }
-    kern<<<(unsigned)p.g.n_items, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv);
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || sms < 1) {
+            snprintf(msg, msg_len, "SM count: %s", cudaGetErrorString(e));
+            sms = 0;
+            return MERCURY_ECUDA;
+        }
+    }
+    // persistent: one CTA per SM (the shared memory and TMEM use allow one)
+    const long long grid = p.g.n_items < sms ? p.g.n_items : sms;
+    if (grid < 1)
+        return MERCURY_OK;
+    kern<<<(unsigned)grid, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "attention kernel launch: %s", cudaGetErrorString(e));
