@@ -273,20 +273,23 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     c.d = d;
     c.R = R;
     c.causal = causal ? 1 : 0;
-    c.mode = partial ? kPerStep : (groups > 1 ? kGrouped : kFused);
-    c.n_groups = partial ? R : groups;
+    // One run per step is the per-step split: use its shard-major item order
+    // (resident CTAs then read the same shard, which matters once K/V
+    // outgrow L2); the merge does not depend on the slot order.
+    c.mode = (partial || groups >= R) ? kPerStep : (groups > 1 ? kGrouped : kFused);
+    c.n_groups = (partial || groups >= R) ? R : groups;
     c.order = order;
     c.out = out;
     c.lse = lse;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
-    if (c.mode != kGrouped) {
+    if (partial || c.mode == kFused) {
         rc = launch_attention(c, s, g_msg, sizeof g_msg);
         return finish(rc, s);
     }
     // split-KV: partials of every run into pooled scratch, then the merge
     Geom g;
-    make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, kGrouped, groups);
+    make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, c.mode, c.n_groups);
     const long long rows = (long long)B * Hq * Sq;
     const size_t o_bytes = (size_t)g.n_groups * rows * d * sizeof(float);
     const size_t l_bytes = (size_t)g.n_groups * rows * sizeof(float);
