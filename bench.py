@@ -354,6 +354,11 @@ def run_gpu(args):
         secondary = measure_merge_path(m, dev, stream, peaks, peak_kind)
         torch.cuda.empty_cache()
 
+    gemm = None
+    if not args.no_secondary and rank == 0 and world == 1:
+        gemm = measure_gemm(m, dev, stream, peaks, peak_kind)
+        torch.cuda.empty_cache()
+
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         rate, n, dt, sample = oracle_rate(q, k, v, w, seconds=args.cpu_seconds, seed=w["seed"])
@@ -375,7 +380,7 @@ def run_gpu(args):
                            (q.numel() + k.numel() + v.numel()) * 2 >> 20)},
             "gpu_launches": args.steps * launches_per_step,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "secondary": secondary,
+            "secondary": secondary, "gemm": gemm,
             "per_step_ms": {"min": round(min(per_step_ms), 4), "median": round(statistics.median(per_step_ms), 4),
                             "max": round(max(per_step_ms), 4)},
         }
@@ -439,6 +444,33 @@ def measure_merge_path(m, dev, stream, peaks, peak_kind, reps: int = 10):
             "sharded_auto_ms": round(statistics.median(t_sh) * 1e3, 4),
             "sharded_auto_tflops": round(flops / statistics.median(t_sh) / 1e12, 2),
             "peak_kind": peak_kind, "reps": reps}
+
+
+def measure_gemm(m, dev, stream, peaks, peak_kind, reps: int = 10):
+    """The shifted-shard GEMM (all-gather GEMM pattern) on its workload: TFLOP/s
+    of mercury_gemm_shifted (2*M*N*K flop per call)."""
+    import torch
+
+    from long_context_sharded_gb300.workloads import GEMM_WORKLOADS
+    name = "gemm_m16k_k8k_n28k_r8"
+    w = GEMM_WORKLOADS[name]
+    g = torch.Generator().manual_seed(w["seed"])
+    a = (torch.randn((w["M"], w["K"]), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    b = (torch.randn((w["K"], w["N"]), generator=g) * 0.5).to(torch.bfloat16).to(dev)
+    c = torch.empty((w["M"], w["N"]), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        m.mercury_gemm_shifted(a, b, w["R"], w["shift"], c, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        m.mercury_gemm_shifted(a, b, w["R"], w["shift"], c, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    m.mercury_sync_status(stream)
+    t = e0.elapsed_time(e1) / reps / 1e3
+    flops = 2.0 * w["M"] * w["N"] * w["K"]
+    return {"workload": name, "ms": round(t * 1e3, 4), "tflops": round(flops / t / 1e12, 2),
+            "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 4), "peak_kind": peak_kind, "reps": reps}
 
 
 # --------------------------------------------------------- reference arm

@@ -149,6 +149,26 @@ MERCURY_API int mercury_lse_merge(const float *o_part, const float *lse_part, in
                       long long rows, int d, float *out, float *lse, void *stream);
 
 /*
+ * mercury_gemm_shifted -- the all-gather GEMM pattern under the shifted
+ * schedule (the pages' second operator family: every rank owns a slice of A
+ * while all ranks need B, and B's pieces are read from their owners in a
+ * rank-staggered order; Silicon & Systems, "The hidden cost of synchronized
+ * operators" and "What Mercury finds that templates miss").
+ *
+ * R virtual ranks: rank i owns the row block A_i = rows [i*M/R, (i+1)*M/R) of
+ * A; B is cut into R column shards B_s = columns [s*N/R, (s+1)*N/R); at step j
+ * rank i computes C[block i, shard order[i][j]] = A_i B_s, order as in
+ * mercury_plan_shift(R, shift).  The result is C = A B.
+ * a [M,K] bf16, b [K,N] bf16, c [M,N] fp32, all row-major device pointers,
+ * 16-byte aligned, caller-owned.  Requirements: M, N, K >= 1; R divides M and
+ * N; N/R and K multiples of 8; valid (R, shift).
+ * Errors: MERCURY_EINVAL, MERCURY_EALIGN, MERCURY_ECUDA, and
+ * MERCURY_ETIMEOUT when MERCURY_SYNC_CHECK=1.
+ */
+MERCURY_API int mercury_gemm_shifted(const void *a, const void *b, int M, int N, int K,
+                                     int R, int shift, float *c, void *stream);
+
+/*
  * mercury_attn_split_noalloc -- mercury_attn_sharded's split-KV schedule for
  * callers that cannot allocate device memory.  (The pages have no
  * counterpart: this is a deployment convenience of this library.)

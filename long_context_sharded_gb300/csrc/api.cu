@@ -119,17 +119,28 @@ int check_attn_args(const void *q, const void *k, const void *v, int B, int Hq, 
     return MERCURY_OK;
 }
 
+// Synchronise `stream` and collect the error words of every kernel module.
+int collect_device_errors(cudaStream_t stream)
+{
+    unsigned int w = 0, site = 0, w2 = 0, site2 = 0;
+    int rc = read_and_clear_device_error(stream, &w, &site, g_msg, sizeof g_msg);
+    if (rc == MERCURY_OK)
+        rc = read_and_clear_gemm_error(&w2, &site2, g_msg, sizeof g_msg);
+    if (rc != MERCURY_OK)
+        return rc;
+    if ((w | w2) & 1u)
+        return fail(MERCURY_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", (w & 1u) ? site : site2);
+    return MERCURY_OK;
+}
+
 int finish(int rc, cudaStream_t stream)
 {
     if (rc != MERCURY_OK)
         return rc;
     if (sync_check()) {
-        unsigned int w = 0, site = 0;
-        rc = read_and_clear_device_error(stream, &w, &site, g_msg, sizeof g_msg);
+        rc = collect_device_errors(stream);
         if (rc != MERCURY_OK)
             return rc;
-        if (w & 1u)
-            return fail(MERCURY_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", site);
     }
     return ok();
 }
@@ -376,14 +387,38 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
     return finish(rc, s);
 }
 
+int mercury_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R, int shift, float *c,
+                         void *stream)
+{
+    if (!a || !b || !c)
+        return fail(MERCURY_EINVAL, "null pointer argument");
+    if (M < 1 || N < 1 || K < 1)
+        return fail(MERCURY_EINVAL, "M, N, K must be >= 1");
+    int rc = check_shift(R, shift);
+    if (rc)
+        return rc;
+    if (M % R != 0 || N % R != 0)
+        return fail(MERCURY_EINVAL, "R (%d) must divide M (%d) and N (%d)", R, M, N);
+    if ((N / R) % 8 != 0 || K % 8 != 0)
+        return fail(MERCURY_EINVAL, "N/R and K must be multiples of 8 (N/R %d, K %d)", N / R, K);
+    long long n = 1;
+    if (!mul_ok(n, M) || !mul_ok(n, N) || !mul_ok(n, 4) || (long long)M * K > (1LL << 62) / 2 ||
+        (long long)K * N > (1LL << 62) / 2)
+        return fail(MERCURY_EINVAL, "tensor sizes overflow");
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16))
+        return fail(MERCURY_EALIGN, "a, b and c must be 16-byte aligned");
+    int order[kMaxR * kMaxR];
+    plan_shift(R, shift, order);
+    cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_gemm_shifted(a, b, M, N, K, R, order, c, wait_budget_ns(), s, g_msg, sizeof g_msg);
+    return finish(rc, s);
+}
+
 int mercury_sync_status(void *stream)
 {
-    unsigned int w = 0, site = 0;
-    int rc = read_and_clear_device_error((cudaStream_t)stream, &w, &site, g_msg, sizeof g_msg);
+    int rc = collect_device_errors((cudaStream_t)stream);
     if (rc != MERCURY_OK)
         return rc;
-    if (w & 1u)
-        return fail(MERCURY_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", site);
     return ok();
 }
 

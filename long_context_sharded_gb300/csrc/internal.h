@@ -30,6 +30,14 @@ int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int H
                        int d, int R, int shift, int causal, int n_runs, float *out, float *lse,
                        cudaStream_t stream, char *msg, size_t msg_len);
 
+// Shifted-shard GEMM: C [M,N] fp32 = A [M,K] bf16 x B [K,N] bf16; rank i's
+// row block against B's column shards in the order order[i][*].
+int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R, const int *order, float *c,
+                        unsigned long long wait_ns, cudaStream_t stream, char *msg, size_t msg_len);
+
+// Read and clear the GEMM kernel's device error word (no synchronisation).
+int read_and_clear_gemm_error(unsigned int *word, unsigned int *site, char *msg, size_t msg_len);
+
 // Synchronise `stream`, read and clear the kernels' device error word.
 int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,
                                 size_t msg_len);

@@ -38,7 +38,8 @@ _STATUS_NAMES = {
 # Every symbol include/mercury_attn.h declares.
 EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial",
             "mercury_lse_merge", "mercury_sync_status", "mercury_last_error",
-            "mercury_work_decomposition", "mercury_work_item_rows", "mercury_attn_split_noalloc")
+            "mercury_work_decomposition", "mercury_work_item_rows", "mercury_attn_split_noalloc",
+            "mercury_gemm_shifted")
 
 
 class MercuryError(RuntimeError):
@@ -60,6 +61,7 @@ def _load() -> ctypes.CDLL:
     lib.mercury_attn_sharded.argtypes = attn_args
     lib.mercury_attn_partial.argtypes = attn_args
     lib.mercury_lse_merge.argtypes = [p, p, i32, i64, i32, p, p, p]
+    lib.mercury_gemm_shifted.argtypes = [p, p, i32, i32, i32, i32, i32, p, p]
     lib.mercury_attn_split_noalloc.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                                i32, p, p, p]
     lib.mercury_sync_status.argtypes = [p]
@@ -190,6 +192,21 @@ def mercury_attn_split_noalloc(q, k, v, R: int, shift: int, causal: bool, n_runs
         _stream_ptr(stream))
     _check(rc)
     return out, lse
+
+
+def mercury_gemm_shifted(a, b, R: int, shift: int, c=None, stream=None):
+    """C = A @ B through the shifted schedule: a [M,K], b [K,N] bf16 -> c [M,N] fp32."""
+    import torch
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError("a [M,K] and b [K,N] expected")
+    M, K = a.shape
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    rc = lib.mercury_gemm_shifted(_dev_ptr(a, "torch.bfloat16", "a"), _dev_ptr(b, "torch.bfloat16", "b"),
+                                  M, N, K, R, shift, _dev_ptr(c, "torch.float32", "c"), _stream_ptr(stream))
+    _check(rc)
+    return c
 
 
 def mercury_sync_status(stream=None) -> None:

@@ -60,3 +60,11 @@ def attention_flops(w: dict) -> int:
     """Algorithmic FLOPs: 4*d per unmasked (q, k) pair (2*d for the score, 2*d
     for the value sum), over all batches and query heads."""
     return 4 * w["d"] * w["B"] * w["Hq"] * unmasked_pairs(w["Sq"], w["Skv"], w["causal"])
+
+
+# The all-gather GEMM pattern (the pages' second operator family, batch 16):
+# a Llama-3-70B-like MLP projection, 16 x 1024 tokens x 8192 hidden -> 28672,
+# R = 8 virtual ranks each owning a row block of A, B cut into 8 column shards.
+GEMM_WORKLOADS = {
+    "gemm_m16k_k8k_n28k_r8": dict(M=16384, K=8192, N=28672, R=8, shift=1, seed=6),
+}
