@@ -173,8 +173,11 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     // tensor-memory columns of S_t and O_t
     auto col_s = [](int t) { return (uint32_t)(t * 128); };
     auto col_o = [](int t) { return (uint32_t)(256 + t * D); };
-    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kTileKeys, false);
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+    // cta_group::1 kind::f16: M = 128, N a multiple of 16 up to 256
+    static_assert(kTileRows == 128 && kTileKeys % 16 == 0 && kTileKeys <= 256 && D % 16 == 0 && D <= 256,
+                  "MMA shape");
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileRows, kTileKeys, false);
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileRows, D, true);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);

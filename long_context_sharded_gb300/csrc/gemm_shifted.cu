@@ -10,15 +10,17 @@
 // rank i at step j computes C[block i, shard order[i][j]] = A_i B_s.  The
 // result is C = A B, fp32, from bf16 inputs.
 //
-// Kernel: persistent, one CTA per SM walking output tiles of 128 x 256 in
+// Kernel: persistent, one CTA per SM walking output tiles of 256 x 256 in
 // step-major order (step j, rank i, then the tiles of that (rank, shard)
 // block), so the CTAs resident together share one A block and one B shard in
-// L2.  Warp 0: TMA producer (A tile 128 x 64, K-major; B tile 64 x 256 as
-// four 64-column boxes, N-major) into a 4-stage ring.  Warp 1: one thread
-// issues tcgen05.mma kind::f16, M = 128, N = 256, K = 16 (128 tensor cycles
-// per instruction, well above the issue cost of an MMA) into one of two
-// 256-column TMEM accumulators.  Warps 4-7: epilogue, TMEM -> fp32 global,
-// overlapping the next tile's MMAs (double-buffered accumulators).
+// L2.  Warp 0: TMA producer (A tile 256 x 64 as two 128-row boxes, K-major;
+// B tile 64 x 256 as four 64-column boxes, N-major) into a 3-stage ring:
+// 64 KB per 1024 tensor cycles, two thirds of what 128 x 256 tiles pull from
+// L2 per FLOP.  Warp 1: one thread issues tcgen05.mma kind::f16, M = 128,
+// N = 256, K = 16 (128 tensor cycles per instruction, well above the issue
+// cost of an MMA) into two 256-column TMEM accumulators, one per 128-row
+// half.  Warps 4-7 and 8-11: epilogue of the two halves, TMEM -> fp32 global;
+// the first half drains while the second half's last MMAs run.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,10 +41,14 @@ __device__ unsigned int g_gemm_err_site = 0;
 
 namespace {
 
-constexpr int kGThreads = 256;
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kGThreads = 384;
+constexpr int kBM = 256, kBN = 256, kBK = 64;  // CTA tile (two 128-row halves)
+constexpr int kMmaM = 128;                     // M of one tcgen05.mma (cta_group::1)
+static_assert(kMmaM == 128, "cta_group::1 kind::f16 MMAs here are M = 128");
+static_assert(kBM == 2 * kMmaM, "the CTA tile is two MMA halves");
+constexpr int kStages = 3;
+constexpr int kAHalf = kMmaM * kBK * 2;  // 16 KB: one 128-row half of A
+constexpr int kABytes = 2 * kAHalf;      // 32 KB
 constexpr int kBBytes = kBK * kBN * 2;   // 32 KB: four 64 x 64 boxes of 8 KB
 constexpr int kBBox = kBK * 64 * 2;      // 8 KB
 constexpr int kGOffBar = kStages * (kABytes + kBBytes);
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB)
 {
-    constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true);  // B is N-major
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kMmaM, kBN, true);  // B is N-major
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
@@ -129,7 +135,7 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(acc_full + a, 1);
-            mbar_init(acc_empty + a, 4);  // one arrive per epilogue warp
+            mbar_init(acc_empty + a, 4);  // one arrive per warp of that half's epilogue
         }
         *abort_flag = 0u;
         fence_mbar_init();
@@ -159,8 +165,9 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     break;
                 }
                 mbar_arrive_expect_tx(full + st, (uint32_t)(kABytes + kBBytes));
-                // A tile: [128 rows][64 k], box {64, 128} at (k, m)
+                // A tile: [256 rows][64 k] as two boxes {64, 128} at (k, m), (k, m + 128)
                 tma_load_2d(sA + st * kABytes, &tmA, full + st, kb * kBK, t.m0);
+                tma_load_2d(sA + st * kABytes + kAHalf, &tmA, full + st, kb * kBK, t.m0 + 128);
                 // B tile: [64 k][256 n] as four boxes {64 n, 64 k}
                 for (int c = 0; c < kBN / 64; ++c)
                     tma_load_2d(sB + st * kBBytes + c * kBBox, &tmB, full + st, t.n0 + c * 64, kb * kBK);
@@ -175,46 +182,49 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
         int it = 0, tile = 0;
         bool ok = true;
         for (long long idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x, ++tile) {
-            const int acc = tile & 1;
-            // the accumulator's previous tile must have been read out
-            if (tile >= 2 && !gwait(acc_empty + acc, ((tile >> 1) - 1) & 1, p.wait_ns, abort_flag, 0x402)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + acc * kBN;
-            for (int kb = 0; kb < p.KB; ++kb, ++it) {
+            for (int kb = 0; kb < p.KB && ok; ++kb, ++it) {
                 const int st = it % kStages;
                 if (!gwait(full + st, (it / kStages) & 1, p.wait_ns, abort_flag, 0x403)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t das = da + ((uint32_t)(st * kABytes) >> 4);
                 const uint64_t dbs = db + ((uint32_t)(st * kBBytes) >> 4);
+                for (int h = 0; h < 2; ++h) {
+                    // this half's accumulator must have been read out (previous tile)
+                    if (kb == 0 && tile >= 1 &&
+                        !gwait(acc_empty + h, (tile - 1) & 1, p.wait_ns, abort_flag, 0x402)) {
+                        ok = false;
+                        break;
+                    }
+                    if (kb == 0)
+                        tc_fence_after();
+                    const uint64_t das = da + ((uint32_t)(st * kABytes + h * kAHalf) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    umma_ss(d, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)), kIdesc,
-                            (kb > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(empty + st);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        umma_ss(tmem + h * kBN, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)),
+                                kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    if (kb == p.KB - 1)
+                        umma_commit(acc_full + h);  // this half is final: its epilogue may start
+                }
+                if (ok)
+                    umma_commit(empty + st);
             }
-            if (ok)
-                umma_commit(acc_full + acc);
         }
         // let the last stage releases land before the CTA exits
         for (int m = (it > kStages ? it - kStages : 0); m < it && ok; ++m)
             ok = gwait(empty + (m % kStages), (m / kStages) & 1, p.wait_ns, abort_flag, 0x404);
     } else if (warp >= 4) {
         // ----------------------------------------------------- epilogue
+        const int acc = (warp - 4) / 4;  // the 128-row half this warpgroup writes
         const int quarter = warp % 4;
-        const int r = quarter * 32 + lane;
+        const int r = acc * 128 + quarter * 32 + lane;
         const uint32_t lane_field = (uint32_t)(quarter * 32) << 16;
         int tile = 0;
         bool ok = true;
         for (long long idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x, ++tile) {
             const GTile t = decode_gtile(p, idx);
-            const int acc = tile & 1;
-            bool got = gwait(acc_full + acc, (tile >> 1) & 1, p.wait_ns, abort_flag, 0x405);
+            bool got = gwait(acc_full + acc, tile & 1, p.wait_ns, abort_flag, 0x405);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
@@ -313,7 +323,11 @@ int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R
     for (int i = 0; i < R * R; ++i)
         p.order[i] = (unsigned char)order[i];
     CUtensorMap ma, mb;
-    int rc = encode_2d(&ma, a, (uint64_t)K, (uint64_t)M, kBK, kBM, msg, msg_len);
+    // A is loaded as two 128-row boxes per stage, B as four 64-column boxes:
+    // the boxes must add up to the bytes each stage's barrier expects
+    static_assert(kAHalf == kBK * kMmaM * 2 && kABytes == 2 * kAHalf, "A box");
+    static_assert(kBBox == 64 * kBK * 2 && kBBytes == (kBN / 64) * kBBox, "B box");
+    int rc = encode_2d(&ma, a, (uint64_t)K, (uint64_t)M, kBK, kMmaM, msg, msg_len);
     if (rc == MERCURY_OK)
         rc = encode_2d(&mb, b, (uint64_t)N, (uint64_t)K, 64, kBK, msg, msg_len);
     if (rc != MERCURY_OK)

@@ -166,9 +166,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major, B K-major or MN-major (bit 16),
 // N >> 3 in bits [17,23), M >> 4 in bits [24,29).
+// Not constexpr: a descriptor for an unsupported shape cannot be a compile-time
+// constant, so `constexpr uint32_t d = idesc_bf16_f32(...)` fails to compile.
+__host__ __device__ inline uint32_t unsupported_mma_shape()
+{
+    return 0u;
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+    // only the cta_group::1 shapes used here: M 128, N a multiple of 16 in [16, 256]
+    return (M != 128 || N % 16 != 0 || N < 16 || N > 256) ? unsupported_mma_shape() : (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
