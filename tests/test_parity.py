@@ -110,6 +110,9 @@ SMALL = [
     (1, 6, 3, 64, 192, 128, 8, 2, True),       # Bq = 8, Sq < Skv causal, nested
     (1, 4, 1, 16, 16, 128, 1, 1, True),        # tiny
     (1, 2, 2, 1000, 1000, 128, 1, 1, True),    # Skv not a multiple of 128
+    (1, 2, 2, 1024, 1024, 64, 128, 1, True),   # the largest R: 8-row blocks and shards
+    (1, 4, 1, 512, 2048, 128, 4, 1, True),     # causal, Sq < Skv (bottom-right alignment)
+    (3, 4, 4, 640, 640, 128, 5, 1, False),     # odd batch and R
 ]
 
 
@@ -193,7 +196,8 @@ def test_output_canaries_untouched(m):
 # ------------------------------------------------------ merge kernel
 
 @pytest.mark.parametrize("n_parts,rows,d", [(1, 7, 128), (4, 33, 64), (64, 1000, 128),
-                                            (3, 5, 4), (130, 17, 256), (8, 64, 12)])
+                                            (3, 5, 4), (130, 17, 256), (8, 64, 12), (4096, 3, 128),
+                                            (2, 1, 512)])
 def test_lse_merge_matches_oracle(m, n_parts, rows, d):
     g = torch.Generator().manual_seed(n_parts * 1000 + rows)
     o = torch.randn(n_parts, rows, d, generator=g)
