@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "351975c183be6b8d", "bytes_per_launch": 2577907712,
+ATTN_TRAFFIC = {"source_sha": "7dcfa532db602f46", "bytes_per_launch": 2429332608,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
