@@ -149,6 +149,26 @@ MERCURY_API int mercury_lse_merge(const float *o_part, const float *lse_part, in
                       long long rows, int d, float *out, float *lse, void *stream);
 
 /*
+ * mercury_attn_decode -- attention for a short query side against a long KV
+ * (decode and chunked-prefill shapes), split across the KV.
+ *
+ * The whole query side [B,Hq,Sq,d] is one block (one rank); the KV is cut
+ * into n_splits contiguous shards, each shard's partial (O, LSE) is computed
+ * on its own work items (which fills the GPU when B*Hq*Sq is small) into
+ * scratch memory from the library's per-device pool, and the partials are
+ * combined by the log-sum-exp merge of mercury_lse_merge.  The result equals
+ * softmax(QK^T/sqrt(d))V; causal alignment as elsewhere (k <= q + Skv - Sq).
+ * n_splits: 1..128 dividing Skv, or 0 to choose the smallest divisor of Skv
+ * that gives every SM four work items.  Scratch: n_splits * B*Hq*Sq*(d+1)*4
+ * bytes.  Other arguments, layouts and errors as mercury_attn_sharded
+ * (Sq need not be divisible by anything).
+ */
+MERCURY_API int mercury_attn_decode(const void *q, const void *k, const void *v,
+                                    int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                    int n_splits, int causal, float *out, float *lse,
+                                    void *stream);
+
+/*
  * mercury_gemm_shifted -- the all-gather GEMM pattern under the shifted
  * schedule (the pages' second operator family: every rank owns a slice of A
  * while all ranks need B, and B's pieces are read from their owners in a

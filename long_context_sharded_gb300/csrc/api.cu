@@ -289,6 +289,7 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     // outgrow L2); the merge does not depend on the slot order.
     c.mode = (partial || groups >= R) ? kPerStep : (groups > 1 ? kGrouped : kFused);
     c.n_groups = (partial || groups >= R) ? R : groups;
+    c.Rq = R;
     c.order = order;
     c.out = out;
     c.lse = lse;
@@ -384,6 +385,87 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
     cudaStream_t s = (cudaStream_t)stream;
     int rc = attn_split_noalloc(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_runs, out, lse, s,
                                 g_msg, sizeof g_msg);
+    return finish(rc, s);
+}
+
+int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
+                        int d, int n_splits, int causal, float *out, float *lse, void *stream)
+{
+    if (n_splits < 0 || n_splits > kMaxR)
+        return fail(MERCURY_EINVAL, "n_splits must be in [0, %d] (got %d)", kMaxR, n_splits);
+    if (n_splits > 0 && Skv % n_splits != 0)
+        return fail(MERCURY_EINVAL, "n_splits (%d) must divide Skv (%d)", n_splits, Skv);
+    // the argument checks of a one-block call (Sq is not split)
+    int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, 1, 0, causal, out, lse, 0);
+    if (rc)
+        return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    int splits = n_splits;
+    if (splits == 0) {
+        // smallest divisor of Skv (<= 128) that gives every SM four work items
+        int sms = 0;
+        rc = sm_count(&sms);
+        if (rc)
+            return rc;
+        Geom g1;
+        if (make_geom(g1, B, Hq, Hkv, Sq, Skv, d, 1, causal, kFused, 1, 1))
+            return fail(MERCURY_EINVAL, "unsupported shape");
+        splits = 1;
+        for (int c = 1; c <= kMaxR; ++c) {
+            if (Skv % c)
+                continue;
+            splits = c;
+            if (g1.n_items * c >= 4LL * sms)
+                break;
+        }
+    }
+    int order[kMaxR * kMaxR];
+    plan_shift(splits, 1, order);  // rank 0 reads shard j at step j
+    AttnCall c;
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.B = B;
+    c.Hq = Hq;
+    c.Hkv = Hkv;
+    c.Sq = Sq;
+    c.Skv = Skv;
+    c.d = d;
+    c.R = splits;
+    c.Rq = 1;
+    c.causal = causal ? 1 : 0;
+    c.mode = splits == 1 ? kFused : kPerStep;
+    c.n_groups = splits;
+    c.order = order;
+    c.wait_ns = wait_budget_ns();
+    c.fault = fault_mode();
+    if (splits == 1) {
+        c.out = out;
+        c.lse = lse;
+        rc = launch_attention(c, s, g_msg, sizeof g_msg);
+        return finish(rc, s);
+    }
+    const long long rows = (long long)B * Hq * Sq;
+    const size_t o_bytes = (size_t)splits * rows * d * sizeof(float);
+    const size_t l_bytes = (size_t)splits * rows * sizeof(float);
+    cudaMemPool_t pool;
+    rc = scratch_pool(&pool);
+    if (rc)
+        return rc;
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes, pool, s);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "decode split scratch (%zu bytes): %s", o_bytes + l_bytes, cudaGetErrorString(e));
+    float *o_part = (float *)scratch;
+    float *l_part = (float *)((char *)scratch + o_bytes);
+    c.out = o_part;
+    c.lse = l_part;
+    rc = launch_attention(c, s, g_msg, sizeof g_msg);
+    if (rc == MERCURY_OK)
+        rc = launch_lse_merge(o_part, l_part, splits, rows, d, out, lse, s, g_msg, sizeof g_msg);
+    e = cudaFreeAsync(scratch, s);
+    if (rc == MERCURY_OK && e != cudaSuccess)
+        rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
     return finish(rc, s);
 }
 

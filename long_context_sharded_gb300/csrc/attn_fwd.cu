@@ -707,7 +707,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     // storage: the launch path makes no heap allocation.
     static thread_local AttnParams p;
     memset(&p, 0, sizeof p);
-    if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups)) {
+    if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups, c.Rq)) {
         snprintf(msg, msg_len, "unsupported shape");
         return MERCURY_EINVAL;
     }

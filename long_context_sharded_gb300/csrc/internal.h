@@ -13,6 +13,7 @@ struct AttnCall {
     int B, Hq, Hkv, Sq, Skv, d, R, causal;
     int mode;          // kFused, kPerStep or kGrouped (work.h)
     int n_groups;      // kGrouped: runs of steps per rank
+    int Rq;            // query blocks: R, or 1 for a decode split
     const int *order;  // [R*R] shift table from the planner
     float *out, *lse;  // fused: out/lse; otherwise [slots][B,Hq,Sq,(d)] partials
     unsigned long long wait_ns;

@@ -150,6 +150,7 @@ int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int H
     c.causal = causal ? 1 : 0;
     c.mode = kGrouped;
     c.n_groups = n_runs;
+    c.Rq = R;
     c.order = order;
     c.out = o_part;
     c.lse = l_part;

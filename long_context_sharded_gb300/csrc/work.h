@@ -37,6 +37,7 @@ enum Mode { kFused = 0, kPerStep = 1, kGrouped = 2 };
 
 struct Geom {
     int B, Hq, Hkv, Sq, Skv, d, R, causal, partial;  // partial: mode (Mode)
+    int Rq;         // ranks that own query blocks: R, or 1 for a decode split
     int n_groups;   // kGrouped: runs per rank; else 1 (fused) or R (per step)
     int spg;        // steps per run (kGrouped), R (fused), 1 (per step)
     int G;          // query heads per KV head
@@ -52,18 +53,23 @@ struct Geom {
 // Choose the tile geometry.  mode: kFused, kPerStep or kGrouped (then
 // n_groups in [1, R] runs; the run length is ceil(R / n_groups) steps and the
 // run count is recomputed from it).  Returns 0, or -1 when unsupported.
+// Rq: number of query blocks (ranks owning queries); R by default.  A decode
+// split uses Rq = 1: the whole (short) query side is rank 0's, the KV is cut
+// into R shards.
 inline int make_geom(Geom &g, int B, int Hq, int Hkv, int Sq, int Skv, int d, int R,
-                     int causal, int mode, int n_groups = 1)
+                     int causal, int mode, int n_groups = 1, int Rq = -1)
 {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || R < 1 || R > kMaxR)
+    if (Rq < 0)
+        Rq = R;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || R < 1 || R > kMaxR || Rq < 1 || Rq > R)
         return -1;
-    if (Hq % Hkv != 0 || Sq % R != 0 || Skv % R != 0)
+    if (Hq % Hkv != 0 || Sq % Rq != 0 || Skv % R != 0)
         return -1;
     if (mode != kFused && mode != kPerStep && mode != kGrouped)
         return -1;
     if (mode == kGrouped && (n_groups < 1 || n_groups > R))
         return -1;
-    g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.Sq = Sq; g.Skv = Skv; g.d = d; g.R = R;
+    g.B = B; g.Hq = Hq; g.Hkv = Hkv; g.Sq = Sq; g.Skv = Skv; g.d = d; g.R = R; g.Rq = Rq;
     g.causal = causal ? 1 : 0;
     g.partial = mode;
     if (mode == kFused) {
@@ -77,7 +83,7 @@ inline int make_geom(Geom &g, int B, int Hq, int Hkv, int Sq, int Skv, int d, in
         g.n_groups = (R + g.spg - 1) / g.spg;
     }
     g.G = Hq / Hkv;
-    g.Bq = Sq / R;
+    g.Bq = Sq / Rq;
     g.Bk = Skv / R;
     int Mq = kTileRows;
     // pack heads of one group while a tile would otherwise run past its block
@@ -91,7 +97,7 @@ inline int make_geom(Geom &g, int B, int Hq, int Hkv, int Sq, int Skv, int d, in
     g.NHP = g.head_mode ? (g.T_h + 1) / 2 : 1;
     g.NRT = g.head_mode ? g.T_r : (g.T_r + 1) / 2;
     long long per_rank = (long long)g.NHP * g.Hkv * g.B * g.NRT;
-    g.n_items = per_rank * R * (g.partial == kFused ? 1 : g.n_groups);
+    g.n_items = per_rank * Rq * (g.partial == kFused ? 1 : g.n_groups);
     return 0;
 }
 
@@ -122,10 +128,10 @@ MERCURY_HD Item decode_item(const Geom &g, long long idx)
     it.hkv = (int)(idx % g.Hkv); idx /= g.Hkv;
     it.b = (int)(idx % g.B); idx /= g.B;
     int rt = (int)(idx % g.NRT); idx /= g.NRT;
-    int rank = (int)(idx % g.R); idx /= g.R;
+    int rank = (int)(idx % g.Rq); idx /= g.Rq;
     it.shard = g.partial != kFused ? (int)idx : -1;
     if (g.causal && g.partial == kFused) {
-        rank = g.R - 1 - rank;
+        rank = g.Rq - 1 - rank;
         rt = g.NRT - 1 - rt;
     }
     it.rank = rank;

@@ -163,6 +163,23 @@ def test_sharded_auto_split_on_long_kv(m):
     assert_close(out, lse, o_ref, l_ref, "auto split")
 
 
+@pytest.mark.parametrize("cfg", [
+    # B, Hq, Hkv, Sq, Skv, d, n_splits, causal
+    (2, 64, 8, 1, 32768, 128, 0, False),     # Llama-3-70B-like decode step, auto split
+    (1, 32, 32, 4, 8192, 128, 8, False),     # MHA, 4 queries
+    (1, 8, 2, 16, 4096, 64, 0, True),        # causal chunk at the end of the context
+    (1, 8, 1, 3, 3000, 128, 3, True),        # odd lengths, 3 splits
+    (2, 4, 4, 1, 256, 128, 1, False),        # no split (fused)
+], ids=lambda c: "x".join(map(str, c)))
+def test_decode_matches_oracle(m, cfg):
+    B, Hq, Hkv, Sq, Skv, d, n_splits, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:6]))
+    out, lse = m.mercury_attn_decode(q.cuda(), k.cuda(), v.cuda(), n_splits, causal)
+    m.mercury_sync_status()
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "decode")
+
+
 def test_shift_orders_agree_on_gpu(m):
     q, k, v = make_qkv(1, 4, 2, 1024, 1024, 128, seed=42)
     o_ref, l_ref = oracle.attn(q, k, v, True)
