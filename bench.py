@@ -354,9 +354,11 @@ def run_gpu(args):
         secondary = measure_merge_path(m, dev, stream, peaks, peak_kind)
         torch.cuda.empty_cache()
 
-    gemm = None
+    gemm = decode = None
     if not args.no_secondary and rank == 0 and world == 1:
         gemm = measure_gemm(m, dev, stream, peaks, peak_kind)
+        torch.cuda.empty_cache()
+        decode = measure_decode(m, dev, stream, peaks, peak_kind)
         torch.cuda.empty_cache()
 
     cpu = None
@@ -380,7 +382,7 @@ def run_gpu(args):
                            (q.numel() + k.numel() + v.numel()) * 2 >> 20)},
             "gpu_launches": args.steps * launches_per_step,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "secondary": secondary, "gemm": gemm,
+            "secondary": secondary, "gemm": gemm, "decode": decode,
             "per_step_ms": {"min": round(min(per_step_ms), 4), "median": round(statistics.median(per_step_ms), 4),
                             "max": round(max(per_step_ms), 4)},
         }
@@ -471,6 +473,35 @@ def measure_gemm(m, dev, stream, peaks, peak_kind, reps: int = 10):
     flops = 2.0 * w["M"] * w["N"] * w["K"]
     return {"workload": name, "ms": round(t * 1e3, 4), "tflops": round(flops / t / 1e12, 2),
             "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 4), "peak_kind": peak_kind, "reps": reps}
+
+
+def measure_decode(m, dev, stream, peaks, peak_kind, reps: int = 10):
+    """One decode step of a Llama-3-70B-like model at a 128K context, batch 8
+    (64 query / 8 KV heads, d 128, one query per sequence): HBM-bound, so the
+    figure is GB/s of K, V, Q read and O, LSE written.  Inputs are seeded
+    N(0,1) bf16 drawn on the device (4.3 GB of K/V)."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = 8, 64, 8, 1, 131072, 128
+    g = torch.Generator(device=dev).manual_seed(8)
+    q = torch.randn((B, Hq, Sq, d), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, Skv, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, Skv, d), generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        m.mercury_attn_decode(q, k, v, 0, False, out, lse, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        m.mercury_attn_decode(q, k, v, 0, False, out, lse, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    m.mercury_sync_status(stream)
+    t = e0.elapsed_time(e1) / reps / 1e3
+    nbytes = (q.numel() + k.numel() + v.numel()) * 2 + out.numel() * 4 + lse.numel() * 4
+    return {"workload": "decode_b8_hq64_hkv8_d128_skv128k", "ms": round(t * 1e3, 4),
+            "gbs": round(nbytes / t / 1e9, 1), "frac_of_hbm": round(nbytes / t / 1e9 / peaks["hbm_gbs"], 4),
+            "bytes": nbytes, "peak_kind": peak_kind, "reps": reps}
 
 
 # --------------------------------------------------------- reference arm
