@@ -112,6 +112,17 @@ MERCURY_API int mercury_attn_sharded(const void *q, const void *k, const void *v
                          float *out, float *lse, void *stream);
 
 /*
+ * mercury_attn_sharded_bf16 -- mercury_attn_sharded with O written as bf16
+ * (out [B,Hq,Sq,d] bf16, 16-byte aligned; lse stays fp32), halving the output
+ * footprint.  Always the fused schedule (no split-KV scratch).  Arguments,
+ * requirements and errors as mercury_attn_sharded.
+ */
+MERCURY_API int mercury_attn_sharded_bf16(const void *q, const void *k, const void *v,
+                                          int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                          int R, int shift, int causal,
+                                          void *out, float *lse, void *stream);
+
+/*
  * mercury_attn_partial -- the per-step partials of the shifted schedule.
  *
  * For every query row q (virtual rank i = q / (Sq/R)) and step j, slot j of

@@ -388,6 +388,41 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
     return finish(rc, s);
 }
 
+int mercury_attn_sharded_bf16(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq,
+                              int Skv, int d, int R, int shift, int causal, void *out, float *lse, void *stream)
+{
+    int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, (const float *)out, lse, 0);
+    if (rc)
+        return rc;
+    int order[kMaxR * kMaxR];
+    if (plan_shift(R, shift, order))
+        return fail(MERCURY_EINVAL, "invalid (R, shift)");
+    AttnCall c;
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.B = B;
+    c.Hq = Hq;
+    c.Hkv = Hkv;
+    c.Sq = Sq;
+    c.Skv = Skv;
+    c.d = d;
+    c.R = R;
+    c.Rq = R;
+    c.causal = causal ? 1 : 0;
+    c.mode = kFused;
+    c.n_groups = 1;
+    c.order = order;
+    c.out = (float *)out;
+    c.lse = lse;
+    c.out_bf16 = 1;
+    c.wait_ns = wait_budget_ns();
+    c.fault = fault_mode();
+    cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_attention(c, s, g_msg, sizeof g_msg);
+    return finish(rc, s);
+}
+
 int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                         int d, int n_splits, int causal, float *out, float *lse, void *stream)
 {

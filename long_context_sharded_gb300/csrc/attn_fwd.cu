@@ -53,6 +53,7 @@ struct AttnParams {
     Geom g;
     float scale_log2;        // log2(e) / sqrt(d)
     int fault;               // test hook: 1 = drop the first P-ready arrive of tile 0
+    int out_bf16;            // fused calls only: O is written as bf16 ([B,Hq,Sq,d], 2 bytes)
     float *out;              // fused: out; partial: o_part
     float *lse;              // fused: lse; partial: lse_part
     long long slot_o;        // partial: elements between slots of o_part
@@ -573,7 +574,22 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + c0, o);
-                if (orow) {
+                if (orow && p.out_bf16) {
+                    // the row's bf16 elements sit at half the fp32 offset
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        reinterpret_cast<__nv_bfloat16 *>(p.out) + (orow - p.out) + c0);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * c + 2 * e]) * inv,
+                                                                      __uint_as_float(o[8 * c + 2 * e + 1]) * inv);
+                            w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                        }
+                        dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else if (orow) {
                     float4 *dst = reinterpret_cast<float4 *>(orow + c0);
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
@@ -713,6 +729,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     }
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     p.fault = c.fault;
+    p.out_bf16 = c.out_bf16;
     p.out = c.out;
     p.lse = c.lse;
     p.slot_o = (long long)c.B * c.Hq * c.Sq * c.d;

@@ -9,15 +9,16 @@ namespace mercury {
 
 // One attention call, validated by the C-ABI layer.
 struct AttnCall {
-    const void *q, *k, *v;
-    int B, Hq, Hkv, Sq, Skv, d, R, causal;
-    int mode;          // kFused, kPerStep or kGrouped (work.h)
-    int n_groups;      // kGrouped: runs of steps per rank
-    int Rq;            // query blocks: R, or 1 for a decode split
-    const int *order;  // [R*R] shift table from the planner
-    float *out, *lse;  // fused: out/lse; otherwise [slots][B,Hq,Sq,(d)] partials
-    unsigned long long wait_ns;
-    int fault;
+    const void *q = nullptr, *k = nullptr, *v = nullptr;
+    int B = 0, Hq = 0, Hkv = 0, Sq = 0, Skv = 0, d = 0, R = 0, causal = 0;
+    int mode = 0;            // kFused, kPerStep or kGrouped (work.h)
+    int n_groups = 1;        // kGrouped: runs of steps per rank
+    int Rq = 0;              // query blocks: R, or 1 for a decode split
+    const int *order = nullptr;  // [R*R] shift table from the planner
+    float *out = nullptr, *lse = nullptr;  // fused: out/lse; otherwise [slots][B,Hq,Sq,(d)] partials
+    unsigned long long wait_ns = 2000000000ull;
+    int fault = 0;
+    int out_bf16 = 0;        // fused only: out holds bf16 elements
 };
 
 int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len);

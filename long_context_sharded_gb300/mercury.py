@@ -39,7 +39,7 @@ _STATUS_NAMES = {
 EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial",
             "mercury_lse_merge", "mercury_sync_status", "mercury_last_error",
             "mercury_work_decomposition", "mercury_work_item_rows", "mercury_attn_split_noalloc",
-            "mercury_gemm_shifted", "mercury_attn_decode")
+            "mercury_gemm_shifted", "mercury_attn_decode", "mercury_attn_sharded_bf16")
 
 
 class MercuryError(RuntimeError):
@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
     attn_args = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32, p, p, p]
     lib.mercury_plan_shift.argtypes = [i32, i32, p]
     lib.mercury_attn_sharded.argtypes = attn_args
+    lib.mercury_attn_sharded_bf16.argtypes = attn_args
     lib.mercury_attn_partial.argtypes = attn_args
     lib.mercury_lse_merge.argtypes = [p, p, i32, i64, i32, p, p, p]
     lib.mercury_gemm_shifted.argtypes = [p, p, i32, i32, i32, i32, i32, p, p]
@@ -137,6 +138,24 @@ def mercury_attn_sharded(q, k, v, R: int, shift: int, causal: bool, out=None, ls
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
         _dev_ptr(out, "torch.float32", "out"), _dev_ptr(lse, "torch.float32", "lse"),
+        _stream_ptr(stream))
+    _check(rc)
+    return out, lse
+
+
+def mercury_attn_sharded_bf16(q, k, v, R: int, shift: int, causal: bool, out=None, lse=None,
+                              stream=None):
+    """As mercury_attn_sharded, with O returned in bf16 (lse fp32)."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    rc = lib.mercury_attn_sharded_bf16(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+        _dev_ptr(out, "torch.bfloat16", "out"), _dev_ptr(lse, "torch.float32", "lse"),
         _stream_ptr(stream))
     _check(rc)
     return out, lse

@@ -180,6 +180,26 @@ def test_decode_matches_oracle(m, cfg):
     assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "decode")
 
 
+@pytest.mark.parametrize("cfg", [(1, 4, 4, 512, 512, 64, 4, 1, False), (1, 8, 2, 1024, 1024, 128, 8, 4, True),
+                                 (1, 8, 1, 128, 4096, 128, 4, 1, False)], ids=lambda c: "x".join(map(str, c)))
+def test_sharded_bf16_output(m, cfg, monkeypatch):
+    """bf16 O: within the parity tolerance of the oracle, and equal to the fp32
+    fused path's O rounded to bf16 (the fp32 call is held to the fused
+    schedule: a split would round differently)."""
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "1")
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 99)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o16, l16 = m.mercury_attn_sharded_bf16(qd, kd, vd, R, shift, causal)
+    o32, l32 = m.mercury_attn_sharded(qd, kd, vd, R, shift, causal)
+    m.mercury_sync_status()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(o16.float().cpu().numpy(), l16.cpu().numpy(), o_ref, l_ref, "bf16 out")
+
+
 def test_shift_orders_agree_on_gpu(m):
     q, k, v = make_qkv(1, 4, 2, 1024, 1024, 128, seed=42)
     o_ref, l_ref = oracle.attn(q, k, v, True)
