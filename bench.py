@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "7dcfa532db602f46", "bytes_per_launch": 2429332608,
+ATTN_TRAFFIC = {"source_sha": "a892e3eaf7a74f10", "bytes_per_launch": 2559379328,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
@@ -104,7 +104,7 @@ def source_sha(path: str) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 25 ms) of SM clock and throttle reasons."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -121,7 +121,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader", "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader", "-lms", "25"], stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
