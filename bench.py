@@ -353,6 +353,21 @@ def run_gpu(args):
     if not args.no_secondary and rank == 0 and world == 1:
         secondary = measure_merge_path(m, dev, stream, peaks, peak_kind)
         torch.cuda.empty_cache()
+        # the schedule planner's estimates (built-in profile) beside the
+        # measured times of the same schedules
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        prof = m.mercury_default_cost_profile(sms)
+        top = m.mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, 0, prof, 1)[0][0]
+        cw = WORKLOADS[MERGE_WORKLOAD]
+        ctop = m.mercury_plan_schedules(cw["B"], cw["Hq"], cw["Hkv"], cw["Sq"], cw["Skv"], cw["d"], cw["causal"],
+                                        cw["R"], cw["shift"], 0, prof, 1)[0][0]
+        secondary["schedule_model"] = {
+            "bench_workload": {"schedule": [top.R, top.Rq, top.n_runs], "predicted_ms": round(top.predicted_us / 1e3, 4),
+                               "measured_ms": round(statistics.median(per_step_ms), 4)},
+            "merge_workload": {"schedule": [ctop.R, ctop.Rq, ctop.n_runs],
+                               "predicted_ms": round(ctop.predicted_us / 1e3, 4),
+                               "measured_ms_sharded_auto": secondary["sharded_auto_ms"]},
+            "schedule_keys": ["R", "Rq", "n_runs"]}
 
     gemm = decode = None
     if not args.no_secondary and rank == 0 and world == 1:

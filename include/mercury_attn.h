@@ -56,6 +56,7 @@ extern "C" {
 #define MERCURY_ECUDA    (-3)  /* CUDA runtime / driver error (message has details) */
 #define MERCURY_ETIMEOUT (-4)  /* a bounded device wait ran out                     */
 #define MERCURY_ENOMEM   (-5)  /* host-side allocation failed                       */
+#define MERCURY_EBUDGET  (-6)  /* no schedule fits the given device-memory budget   */
 
 /* Largest number of virtual ranks a compute call accepts. */
 #define MERCURY_MAX_R 128
@@ -268,6 +269,149 @@ MERCURY_API int mercury_work_decomposition(int B, int Hq, int Hkv, int Sq, int S
 MERCURY_API int mercury_work_item_rows(int B, int Hq, int Hkv, int Sq, int Skv, int d,
                            int R, int shift, int causal, int mode,
                            long long item, long long *rows, int *n_rows, int *step);
+
+/*
+ * Schedule selection under a device-memory budget.
+ *
+ * The pages make memory capacity part of performance: a schedule that keeps
+ * everything in one piece runs fastest when memory is plentiful, one that
+ * splits its buffers pays extra traffic but can be the only one that fits,
+ * and both should stay available (Silicon & Systems, "Memory capacity is
+ * part of performance").  Candidates are filtered in stages -- a static check
+ * of sizes and divisibility, a cost estimate, then profiling of the best few
+ * on the target device -- and the tuned result is kept under a key of the
+ * device, the library build and the shape, with a re-check when it stops
+ * meeting its measured time (Silicon & Systems, "CommIR makes communication
+ * transformable" and "The tuning bill").
+ *
+ * On one GPU a schedule is the tuple (R, Rq, n_runs, shift):
+ *   R       KV shards (virtual ranks);
+ *   Rq      query blocks: R (virtual rank i owns query block i) or 1 (the
+ *           whole query side is one block that visits all R shards -- the
+ *           query-tile split used for short query sides);
+ *   n_runs  each rank's shifted step sequence is cut into n_runs runs of
+ *           ceil(R / n_runs) consecutive steps; 1 is the fused schedule
+ *           (partials combined on the fly, no scratch), n_runs > 1 writes one
+ *           partial (O, LSE) per run to scratch and merges them as
+ *           mercury_lse_merge does.  Scratch = n_runs * B*Hq*Sq*(d+1)*4 bytes.
+ * The result is the same for every schedule up to rounding.
+ */
+
+/* Costs of this library's kernels on one device (microseconds, GB/s). */
+typedef struct mercury_cost_profile {
+    double tile_us;    /* one 128-key K/V tile through a work item holding two query tiles */
+    double tile1_us;   /* the same for a work item holding one query tile */
+    double item_us;    /* fixed cost of a work item (query load, epilogue) */
+    double launch_us;  /* fixed cost of one attention launch */
+    double merge_gbs;  /* LSE merge throughput: bytes read + written per second / 1e9 */
+    double hbm_gbs;    /* device-to-device copy throughput, GB/s (bytes read + written) */
+    int n_sms;         /* SMs the persistent attention kernel spreads its work items over */
+    int measured;      /* 1: from mercury_measure_cost_profile; 0: built-in GB300 figures */
+} mercury_cost_profile;
+
+/* One candidate schedule and its estimated (and, once profiled, measured) cost. */
+typedef struct mercury_schedule {
+    int R;                    /* KV shards (virtual ranks) */
+    int Rq;                   /* query blocks: R or 1 */
+    int n_runs;               /* runs per rank's step sequence (1 = fused) */
+    int shift;                /* shift order (as in mercury_plan_shift) */
+    long long work_items;     /* attention work items of the launch */
+    long long scratch_bytes;  /* partials of the runs; 0 when n_runs == 1 */
+    long long hbm_bytes;      /* q, k, v, out, lse and scratch together */
+    double predicted_us;      /* cost-model estimate of the whole call */
+    double measured_us;       /* median device time when profiled, else -1 */
+    int pareto;               /* 1: no other candidate of the same call is both
+                                 smaller (hbm_bytes) and predicted faster */
+} mercury_schedule;
+
+/*
+ * mercury_default_cost_profile -- the built-in cost figures (measured on a
+ * GB300 with this library) for a device with n_sms SMs (n_sms >= 1).
+ * Pure host code.  Errors: MERCURY_EINVAL (prof NULL or n_sms < 1).
+ */
+MERCURY_API int mercury_default_cost_profile(int n_sms, mercury_cost_profile *prof);
+
+/*
+ * mercury_measure_cost_profile -- measure the cost figures on the current
+ * device: timed attention launches on synthetic inputs (one and two work
+ * items per SM, two key lengths, one and two query tiles per item), one
+ * timed merge and one timed device-to-device copy, each the median of five
+ * runs after two warm-ups.  The
+ * call allocates about 2 GB of device memory for its inputs, frees it
+ * before returning, and synchronises `stream`.
+ * Errors: MERCURY_EINVAL (prof NULL), MERCURY_ECUDA, MERCURY_ETIMEOUT.
+ */
+MERCURY_API int mercury_measure_cost_profile(mercury_cost_profile *prof, void *stream);
+
+/*
+ * mercury_plan_schedules -- the static filter and the cost estimate (pure
+ * host code, no GPU).
+ *
+ * Enumerates the schedules of an attention call with the shape given: R
+ * fixed (R >= 1) or, with R == 0, every R in 1..MERCURY_MAX_R that divides
+ * Skv and suits `shift` (k >= 2 must divide R); Rq in {R, 1} (R only if it
+ * divides Sq); every distinct n_runs in 1..R.  Drops those whose hbm_bytes
+ * exceed budget_bytes (budget_bytes <= 0: no limit) and estimates the rest:
+ * every work item costs item_us plus its K/V tiles times tile_us (tile1_us
+ * for one query tile), items go to n_sms CTAs round robin in launch order,
+ * and the attention launch costs launch_us plus the larger of the busiest
+ * CTA's sum and its least memory traffic (q, k, v read once, its outputs
+ * written once) at hbm_gbs; when n_runs > 1 a second launch and the merge's
+ * bytes at merge_gbs are added.
+ * Writes the min(count, max_plans) fastest candidates to plans[], fastest
+ * first (ties: fewer hbm_bytes, then Rq == R, then smaller R, then fewer
+ * runs), with the Pareto flag set over all candidates; *n_plans = count.  prof is required (from
+ * mercury_default_cost_profile or mercury_measure_cost_profile).
+ * Requirements: as mercury_attn_sharded for (B, Hq, Hkv, Sq, Skv, d, causal,
+ * shift); max_plans >= 0 (plans may be NULL when it is 0).
+ * Errors: MERCURY_EINVAL; MERCURY_EBUDGET when no candidate fits the budget
+ * (the message states the smallest hbm_bytes of any candidate).
+ */
+MERCURY_API int mercury_plan_schedules(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                                       int R, int shift, long long budget_bytes,
+                                       const mercury_cost_profile *prof,
+                                       mercury_schedule *plans, int max_plans, int *n_plans);
+
+/*
+ * mercury_attn_run_schedule -- attention by a given schedule (one of
+ * mercury_plan_schedules' candidates, or any valid tuple).  Arguments and
+ * layouts as mercury_attn_sharded; the schedule's R, Rq, n_runs and shift
+ * replace R and shift.  The scratch of n_runs > 1 comes stream-ordered from
+ * the library's per-device pool.
+ * Errors: MERCURY_EINVAL (invalid tuple for the shape), MERCURY_EALIGN,
+ * MERCURY_ECUDA, and MERCURY_ETIMEOUT when MERCURY_SYNC_CHECK=1.
+ */
+MERCURY_API int mercury_attn_run_schedule(const void *q, const void *k, const void *v,
+                                          int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                          int causal, const mercury_schedule *plan,
+                                          float *out, float *lse, void *stream);
+
+/*
+ * mercury_tune_schedule -- pick a schedule by measurement and compute the
+ * attention with it.
+ *
+ * Plans the call (mercury_plan_schedules with the profile of
+ * mercury_default_cost_profile for this device), runs the top_k predicted
+ * candidates (1 <= top_k <= 16) on the caller's buffers -- one warm-up and
+ * three timed launches each, CUDA events on `stream`, median -- and keeps the
+ * fastest.  The choice is cached for the process under (device ordinal, SM
+ * count, compute capability, library build, shape, R, shift, budget, top_k).
+ * A later call with the same key runs the cached schedule once, timed; if it
+ * takes more than 1.5 times its recorded time the entry is dropped and the
+ * call tunes again.  On return out / lse hold the attention result (from the
+ * chosen schedule's last run) and *best (if not NULL) the chosen schedule
+ * with measured_us set.  *cache_hit (if not NULL) is 1 when no tuning ran.
+ * The call synchronises `stream`.
+ * Errors: as mercury_plan_schedules and mercury_attn_run_schedule.
+ */
+MERCURY_API int mercury_tune_schedule(const void *q, const void *k, const void *v,
+                                      int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                      int R, int shift, int causal, long long budget_bytes,
+                                      int top_k, float *out, float *lse, void *stream,
+                                      mercury_schedule *best, int *cache_hit);
+
+/* Drop every cached tuning result of mercury_tune_schedule. */
+MERCURY_API void mercury_tune_cache_clear(void);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmercury_attn.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "lse_merge.cu", "noalloc.cu", "gemm_shifted.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "lse_merge.cu", "noalloc.cu", "gemm_shifted.cu", "schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

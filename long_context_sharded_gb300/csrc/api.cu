@@ -183,45 +183,18 @@ long long env_ll(const char *name, long long dflt)
 // whose partials are merged afterwards -- the latency / memory trade the
 // pages describe (Silicon & Systems, "Memory capacity is part of
 // performance"): more runs fill the SMs but cost scratch and merge traffic.
-// A small cost model picks the run count: waves of work items x run length,
-// plus a per-item set-up cost, plus the merge's HBM traffic; scratch is
-// capped at MERCURY_SCRATCH_MAX_BYTES (default 4 GiB).  Returns the number of
-// runs (1 = fused).  MERCURY_SPLIT_GROUPS forces it.
-int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int causal, int sms)
+// The run count is the one schedule.cu's cost model predicts fastest among
+// those whose scratch fits in MERCURY_SCRATCH_MAX_BYTES (default 4 GiB).
+// Returns the number of runs (1 = fused).  MERCURY_SPLIT_GROUPS forces it.
+int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int shift, int causal, int sms)
 {
     long long forced = env_ll("MERCURY_SPLIT_GROUPS", 0);
     if (forced >= 1)
         return (int)(forced < R ? forced : R);
-    Geom g;
-    if (make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, kFused) || sms < 1)
+    if (R == 1 || sms < 1)
         return 1;
-    if (R == 1 || g.n_items >= 4LL * sms)
-        return 1;  // enough items: the fused schedule keeps every SM busy
-    const double t_tile = 1.3e-6;   // one 128-key tile through a two-tile item
-    const double t_item = 4e-6;     // per item: set-up, Q load, epilogue
-    const double merge_bw = 6e12;   // bytes per second of the merge
     const long long cap = env_ll("MERCURY_SCRATCH_MAX_BYTES", 4LL << 30);
-    const double per_slot = (double)B * Hq * Sq * (d + 1) * 4;
-    const double tiles_per_step = (double)((g.Bk + kTileKeys - 1) / kTileKeys);
-    double best = 0;
-    int best_g = 1;
-    for (int gr = 1; gr <= R; ++gr) {
-        const int spg = (R + gr - 1) / gr;
-        if ((R + spg - 1) / spg != gr)
-            continue;  // same runs as a smaller count
-        if (gr > 1 && gr * per_slot > (double)cap)
-            break;
-        const long long items = g.n_items * gr;
-        const long long waves = (items + sms - 1) / sms;
-        double cost = waves * (spg * tiles_per_step * t_tile + t_item);
-        if (gr > 1)
-            cost += (gr + 1) * per_slot / merge_bw;
-        if (gr == 1 || cost < best) {
-            best = cost;
-            best_g = gr;
-        }
-    }
-    return best_g;
+    return best_run_count(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, sms, cap);
 }
 
 // Library-private stream-ordered pool for split-KV scratch (per device;
@@ -254,6 +227,44 @@ int scratch_pool(cudaMemPool_t *pool)
     return MERCURY_OK;
 }
 
+// Run a validated call that produces the final O and LSE: the fused
+// schedule writes them directly; a split schedule (per-step or grouped)
+// writes one partial per slot into pooled scratch and merges the slots.
+int run_to_output(AttnCall &c, float *out, float *lse, cudaStream_t s)
+{
+    if (c.mode == kFused) {
+        c.out = out;
+        c.lse = lse;
+        return launch_attention(c, s, g_msg, sizeof g_msg);
+    }
+    Geom g;
+    if (make_geom(g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups, c.Rq))
+        return fail(MERCURY_EINVAL, "unsupported shape");
+    const long long rows = (long long)c.B * c.Hq * c.Sq;
+    const size_t o_bytes = (size_t)g.n_groups * rows * c.d * sizeof(float);
+    const size_t l_bytes = (size_t)g.n_groups * rows * sizeof(float);
+    cudaMemPool_t pool;
+    int rc = scratch_pool(&pool);
+    if (rc)
+        return rc;
+    void *scratch = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes, pool, s);
+    if (e != cudaSuccess)
+        return fail(MERCURY_ECUDA, "split-KV scratch (%zu bytes): %s", o_bytes + l_bytes,
+                    cudaGetErrorString(e));
+    float *o_part = (float *)scratch;
+    float *l_part = (float *)((char *)scratch + o_bytes);
+    c.out = o_part;
+    c.lse = l_part;
+    rc = launch_attention(c, s, g_msg, sizeof g_msg);
+    if (rc == MERCURY_OK)
+        rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, c.d, out, lse, s, g_msg, sizeof g_msg);
+    e = cudaFreeAsync(scratch, s);
+    if (rc == MERCURY_OK && e != cudaSuccess)
+        rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
+    return rc;
+}
+
 int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                 int d, int R, int shift, int causal, float *out, float *lse, void *stream, int partial)
 {
@@ -270,7 +281,7 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
         rc = sm_count(&sms);
         if (rc)
             return rc;
-        groups = choose_groups(B, Hq, Hkv, Sq, Skv, d, R, causal, sms);
+        groups = choose_groups(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, sms);
     }
     AttnCall c;
     c.q = q;
@@ -291,43 +302,42 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     c.n_groups = (partial || groups >= R) ? R : groups;
     c.Rq = R;
     c.order = order;
-    c.out = out;
-    c.lse = lse;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
-    if (partial || c.mode == kFused) {
+    if (partial) {
+        c.out = out;
+        c.lse = lse;
         rc = launch_attention(c, s, g_msg, sizeof g_msg);
-        return finish(rc, s);
+    } else {
+        rc = run_to_output(c, out, lse, s);
     }
-    // split-KV: partials of every run into pooled scratch, then the merge
-    Geom g;
-    make_geom(g, B, Hq, Hkv, Sq, Skv, d, R, causal, c.mode, c.n_groups);
-    const long long rows = (long long)B * Hq * Sq;
-    const size_t o_bytes = (size_t)g.n_groups * rows * d * sizeof(float);
-    const size_t l_bytes = (size_t)g.n_groups * rows * sizeof(float);
-    cudaMemPool_t pool;
-    rc = scratch_pool(&pool);
-    if (rc)
-        return rc;
-    void *scratch = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes, pool, s);
-    if (e != cudaSuccess)
-        return fail(MERCURY_ECUDA, "split-KV scratch (%zu bytes): %s", o_bytes + l_bytes,
-                    cudaGetErrorString(e));
-    float *o_part = (float *)scratch;
-    float *l_part = (float *)((char *)scratch + o_bytes);
-    c.out = o_part;
-    c.lse = l_part;
-    rc = launch_attention(c, s, g_msg, sizeof g_msg);
-    if (rc == MERCURY_OK)
-        rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, d, out, lse, s, g_msg, sizeof g_msg);
-    e = cudaFreeAsync(scratch, s);
-    if (rc == MERCURY_OK && e != cudaSuccess)
-        rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
     return finish(rc, s);
 }
 
 }  // namespace
+
+namespace mercury {
+
+int set_error(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int clear_error()
+{
+    return ok();
+}
+
+int device_sm_count(int *n)
+{
+    return sm_count(n);
+}
+
+}  // namespace mercury
 
 extern "C" {
 
@@ -474,33 +484,59 @@ int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int 
     c.order = order;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
-    if (splits == 1) {
-        c.out = out;
-        c.lse = lse;
-        rc = launch_attention(c, s, g_msg, sizeof g_msg);
-        return finish(rc, s);
-    }
-    const long long rows = (long long)B * Hq * Sq;
-    const size_t o_bytes = (size_t)splits * rows * d * sizeof(float);
-    const size_t l_bytes = (size_t)splits * rows * sizeof(float);
-    cudaMemPool_t pool;
-    rc = scratch_pool(&pool);
+    rc = run_to_output(c, out, lse, s);
+    return finish(rc, s);
+}
+
+int mercury_attn_run_schedule(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq,
+                              int Skv, int d, int causal, const mercury_schedule *plan, float *out, float *lse,
+                              void *stream)
+{
+    if (!plan)
+        return fail(MERCURY_EINVAL, "plan is NULL");
+    const int R = plan->R, Rq = plan->Rq, runs = plan->n_runs;
+    // the argument checks of a one-block call, then the schedule's own
+    int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, 1, 0, causal, out, lse, 0);
     if (rc)
         return rc;
-    void *scratch = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&scratch, o_bytes + l_bytes, pool, s);
-    if (e != cudaSuccess)
-        return fail(MERCURY_ECUDA, "decode split scratch (%zu bytes): %s", o_bytes + l_bytes, cudaGetErrorString(e));
-    float *o_part = (float *)scratch;
-    float *l_part = (float *)((char *)scratch + o_bytes);
-    c.out = o_part;
-    c.lse = l_part;
-    rc = launch_attention(c, s, g_msg, sizeof g_msg);
-    if (rc == MERCURY_OK)
-        rc = launch_lse_merge(o_part, l_part, splits, rows, d, out, lse, s, g_msg, sizeof g_msg);
-    e = cudaFreeAsync(scratch, s);
-    if (rc == MERCURY_OK && e != cudaSuccess)
-        rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
+    rc = check_shift(R, plan->shift);
+    if (rc)
+        return rc;
+    if (Skv % R != 0)
+        return fail(MERCURY_EINVAL, "R (%d) must divide Skv (%d)", R, Skv);
+    if (Rq != 1 && Rq != R)
+        return fail(MERCURY_EINVAL, "Rq must be 1 or R (Rq %d, R %d)", Rq, R);
+    if (Sq % Rq != 0)
+        return fail(MERCURY_EINVAL, "Rq (%d) must divide Sq (%d)", Rq, Sq);
+    if (runs < 1 || runs > R)
+        return fail(MERCURY_EINVAL, "n_runs must be in [1, R] (n_runs %d, R %d)", runs, R);
+    long long n = 1;
+    if (!mul_ok(n, runs) || !mul_ok(n, B) || !mul_ok(n, Hq) || !mul_ok(n, Sq) || !mul_ok(n, d + 1) ||
+        !mul_ok(n, 4))
+        return fail(MERCURY_EINVAL, "scratch size overflows");
+    int order[kMaxR * kMaxR];
+    plan_shift(R, plan->shift, order);
+    AttnCall c;
+    c.q = q;
+    c.k = k;
+    c.v = v;
+    c.B = B;
+    c.Hq = Hq;
+    c.Hkv = Hkv;
+    c.Sq = Sq;
+    c.Skv = Skv;
+    c.d = d;
+    c.R = R;
+    c.Rq = Rq;
+    c.causal = causal ? 1 : 0;
+    // as mercury_attn_sharded: one run per step takes the shard-major order
+    c.mode = runs == 1 ? kFused : (runs >= R ? kPerStep : kGrouped);
+    c.n_groups = runs >= R ? R : runs;
+    c.order = order;
+    c.wait_ns = wait_budget_ns();
+    c.fault = fault_mode();
+    cudaStream_t s = (cudaStream_t)stream;
+    rc = run_to_output(c, out, lse, s);
     return finish(rc, s);
 }
 

@@ -44,4 +44,17 @@ int read_and_clear_gemm_error(unsigned int *word, unsigned int *site, char *msg,
 int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,
                                 size_t msg_len);
 
+// Status and message of the calling thread, shared by the C-ABI files.
+int set_error(int code, const char *fmt, ...);
+int clear_error();
+
+// SMs of the current device (cached per device).
+int device_sm_count(int *n);
+
+// Run count (1 = fused) with the least estimated time for a call with R
+// virtual ranks each owning a query block, among those whose partials fit in
+// scratch_cap bytes (schedule.cu's cost model, built-in device profile).
+int best_run_count(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int R, int shift, int n_sms,
+                   long long scratch_cap);
+
 }  // namespace mercury

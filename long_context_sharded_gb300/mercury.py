@@ -11,6 +11,9 @@ The functions keep the C names:
   mercury_attn_partial(q, k, v, R, shift, causal, o_part=None, lse_part=None, stream=None)
   mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None)
   mercury_sync_status(stream=None)
+  mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, budget_bytes, profile)
+  mercury_attn_run_schedule(q, k, v, causal, plan, out=None, lse=None, stream=None)
+  mercury_tune_schedule(q, k, v, R, shift, causal, budget_bytes, top_k, ...)
 Tensors: q [B,Hq,Sq,d], k/v [B,Hkv,Skv,d] bf16 CUDA tensors, contiguous.
 """
 from __future__ import annotations
@@ -28,18 +31,45 @@ MERCURY_EALIGN = -2
 MERCURY_ECUDA = -3
 MERCURY_ETIMEOUT = -4
 MERCURY_ENOMEM = -5
+MERCURY_EBUDGET = -6
 MERCURY_MAX_R = 128
 
 _STATUS_NAMES = {
     MERCURY_EINVAL: "EINVAL", MERCURY_EALIGN: "EALIGN", MERCURY_ECUDA: "ECUDA",
-    MERCURY_ETIMEOUT: "ETIMEOUT", MERCURY_ENOMEM: "ENOMEM",
+    MERCURY_ETIMEOUT: "ETIMEOUT", MERCURY_ENOMEM: "ENOMEM", MERCURY_EBUDGET: "EBUDGET",
 }
 
 # Every symbol include/mercury_attn.h declares.
 EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial",
             "mercury_lse_merge", "mercury_sync_status", "mercury_last_error",
             "mercury_work_decomposition", "mercury_work_item_rows", "mercury_attn_split_noalloc",
-            "mercury_gemm_shifted", "mercury_attn_decode", "mercury_attn_sharded_bf16")
+            "mercury_gemm_shifted", "mercury_attn_decode", "mercury_attn_sharded_bf16",
+            "mercury_default_cost_profile", "mercury_measure_cost_profile",
+            "mercury_plan_schedules", "mercury_attn_run_schedule", "mercury_tune_schedule",
+            "mercury_tune_cache_clear")
+
+
+class CostProfile(ctypes.Structure):
+    """mercury_cost_profile: kernel costs of one device (us, GB/s)."""
+    _fields_ = [("tile_us", ctypes.c_double), ("tile1_us", ctypes.c_double),
+                ("item_us", ctypes.c_double), ("launch_us", ctypes.c_double),
+                ("merge_gbs", ctypes.c_double), ("hbm_gbs", ctypes.c_double),
+                ("n_sms", ctypes.c_int), ("measured", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class Schedule(ctypes.Structure):
+    """mercury_schedule: one candidate schedule (R, Rq, n_runs, shift) and its costs."""
+    _fields_ = [("R", ctypes.c_int), ("Rq", ctypes.c_int), ("n_runs", ctypes.c_int),
+                ("shift", ctypes.c_int), ("work_items", ctypes.c_longlong),
+                ("scratch_bytes", ctypes.c_longlong), ("hbm_bytes", ctypes.c_longlong),
+                ("predicted_us", ctypes.c_double), ("measured_us", ctypes.c_double),
+                ("pareto", ctypes.c_int)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class MercuryError(RuntimeError):
@@ -72,9 +102,18 @@ def _load() -> ctypes.CDLL:
     lib.mercury_work_decomposition.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, p]
     lib.mercury_work_item_rows.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                            i64, p, p, p]
+    lib.mercury_default_cost_profile.argtypes = [i32, p]
+    lib.mercury_measure_cost_profile.argtypes = [p, p]
+    lib.mercury_plan_schedules.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i64, p, p,
+                                           i32, p]
+    lib.mercury_attn_run_schedule.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, p, p, p, p]
+    lib.mercury_tune_schedule.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32, i64,
+                                          i32, p, p, p, p, p]
+    lib.mercury_tune_cache_clear.argtypes = []
     for name in EXPORTED:
-        if name != "mercury_last_error":
+        if name not in ("mercury_last_error", "mercury_tune_cache_clear"):
             getattr(lib, name).restype = i32
+    lib.mercury_tune_cache_clear.restype = None
     return lib
 
 
@@ -266,3 +305,79 @@ def mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, mode, item)
                                       int(mode), item, rows, ctypes.byref(n),
                                       ctypes.byref(step)))
     return [rows[i] for i in range(n.value)], step.value
+
+
+def mercury_default_cost_profile(n_sms: int) -> CostProfile:
+    prof = CostProfile()
+    _check(lib.mercury_default_cost_profile(int(n_sms), ctypes.byref(prof)))
+    return prof
+
+
+def mercury_measure_cost_profile(stream=None) -> CostProfile:
+    """Time the kernels on the current device (allocates ~2 GB, synchronises)."""
+    prof = CostProfile()
+    _check(lib.mercury_measure_cost_profile(ctypes.byref(prof), _stream_ptr(stream)))
+    return prof
+
+
+def mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, budget_bytes, profile,
+                           max_plans: int = 512):
+    """Candidates within the budget, fastest predicted first: (list of Schedule, total count)."""
+    plans = (Schedule * max(int(max_plans), 1))()
+    n = ctypes.c_int(0)
+    _check(lib.mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), R, shift,
+                                      int(budget_bytes), ctypes.byref(profile), plans,
+                                      int(max_plans), ctypes.byref(n)))
+    return [plans[i] for i in range(min(n.value, int(max_plans)))], n.value
+
+
+def _schedule(plan):
+    if isinstance(plan, Schedule):
+        return plan
+    s = Schedule()
+    s.R, s.Rq, s.n_runs, s.shift = (int(x) for x in plan)
+    s.measured_us = -1.0
+    return s
+
+
+def mercury_attn_run_schedule(q, k, v, causal: bool, plan, out=None, lse=None, stream=None):
+    """Attention by the schedule `plan` (a Schedule or an (R, Rq, n_runs, shift) tuple)."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    plan = _schedule(plan)
+    rc = lib.mercury_attn_run_schedule(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, int(bool(causal)),
+        ctypes.byref(plan), _dev_ptr(out, "torch.float32", "out"),
+        _dev_ptr(lse, "torch.float32", "lse"), _stream_ptr(stream))
+    _check(rc)
+    return out, lse
+
+
+def mercury_tune_schedule(q, k, v, R: int, shift: int, causal: bool, budget_bytes: int = 0,
+                          top_k: int = 4, out=None, lse=None, stream=None):
+    """Tune by measurement (cached per process); returns (out, lse, Schedule, cache_hit)."""
+    import torch
+    B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    best = Schedule()
+    hit = ctypes.c_int(0)
+    rc = lib.mercury_tune_schedule(
+        _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
+        _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
+        int(budget_bytes), int(top_k), _dev_ptr(out, "torch.float32", "out"),
+        _dev_ptr(lse, "torch.float32", "lse"), _stream_ptr(stream), ctypes.byref(best),
+        ctypes.byref(hit))
+    _check(rc)
+    return out, lse, best, bool(hit.value)
+
+
+def mercury_tune_cache_clear() -> None:
+    lib.mercury_tune_cache_clear()
