@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <map>
 #include <mutex>
 #include <stdio.h>
@@ -362,6 +363,17 @@ namespace mercury {
 int best_run_count(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int R, int shift, int n_sms,
                    long long scratch_cap)
 {
+    // The answer depends only on the arguments; remember it, so a repeated
+    // call does not spend host time on the estimate in front of its launch.
+    static std::mutex mu;
+    static std::map<std::array<long long, 11>, int> memo;
+    const std::array<long long, 11> key = {B, Hq, Hkv, Sq, Skv, d, causal, R, shift, n_sms, scratch_cap};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = memo.find(key);
+        if (it != memo.end())
+            return it->second;
+    }
     mercury_cost_profile p;
     mercury_default_cost_profile(n_sms, &p);
     clear_error();
@@ -380,6 +392,10 @@ int best_run_count(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, i
             best = runs;
         }
     }
+    std::lock_guard<std::mutex> lock(mu);
+    if (memo.size() >= 4096)
+        memo.clear();
+    memo[key] = best;
     return best;
 }
 
