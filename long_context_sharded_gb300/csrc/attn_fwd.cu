@@ -11,9 +11,10 @@
 // Per CTA (one work item, up to two 128-row query tiles sharing a KV head):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles into two
 //               shared-memory rings, in the shifted shard order
-//   warp 1      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V on
-//               the tensor cores (tcgen05.mma kind::f16, fp32 accumulators in
-//               tensor memory); P_t is read straight from tensor memory
+//   warp 1      MMA issuer (the whole warp runs the loop, one elected lane
+//               issues): S_t = Q_t K^T and O_t += P_t V on the tensor cores
+//               (tcgen05.mma kind::f16, fp32 accumulators in tensor
+//               memory); P_t is read straight from tensor memory
 //   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (one query row per
 //               thread): online softmax in the log2 domain, rescaling of O_t
 //               in tensor memory when the running max moves by more than
@@ -294,8 +295,11 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // --------------------------------------------------- MMA issuer
+            // The whole warp runs this loop (its waits and descriptor
+            // arithmetic stay warp-uniform); one elected lane issues each
+            // tcgen05 instruction.
             // Descriptors: the address field (bits 0-13, bytes >> 4) of a base
             // descriptor plus a constant offset never carries out of the field
             // (shared memory < 256 KB), so stepping is one add.
@@ -310,7 +314,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_ss(tmem + col_s(t), da + off, db + off, kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss_w(tmem + col_s(t), da + off, db + off, kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V over K = 128 keys: P_t from tensor memory (bf16 pairs,
@@ -321,7 +325,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 const uint64_t db = dv + ((uint32_t)(sv * L::kKVBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk)
-                    umma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, db + (uint32_t)(kk * (2048 >> 4)),
+                    umma_ts_w(tmem + col_o(t), tmem + col_s(t) + kk * 8, db + (uint32_t)(kk * (2048 >> 4)),
                             kIdescPV, (acc_in || kk > 0) ? 1u : 0u);
             };
             int g = 0;                  // tile-iterations of this CTA so far
@@ -351,7 +355,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     if (n == 0) {
                         for (int t = 0; t < ntile; ++t) {
                             issue_qk(t, sk);
-                            umma_commit(s_full + t);
+                            umma_commit_w(s_full + t);
                             ++sp[t];
                         }
                     } else {
@@ -377,10 +381,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             issue_pv(t, sv, n > 1);
                             if (n < ntot) {
                                 issue_qk(t, sk);
-                                umma_commit(s_full + t);
+                                umma_commit_w(s_full + t);
                                 ++sp[t];
                             } else {
-                                umma_commit(o_full + t);
+                                umma_commit_w(o_full + t);
                                 ++od[t];
                             }
                         }

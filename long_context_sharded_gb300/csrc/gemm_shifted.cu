@@ -16,7 +16,7 @@
 // L2.  Warp 0: TMA producer (A tile 256 x 64 as two 128-row boxes, K-major;
 // B tile 64 x 256 as four 64-column boxes, N-major) into a 3-stage ring:
 // 64 KB per 1024 tensor cycles, two thirds of what 128 x 256 tiles pull from
-// L2 per FLOP.  Warp 1: one thread issues tcgen05.mma kind::f16, M = 128,
+// L2 per FLOP.  Warp 1 (one elected lane) issues tcgen05.mma kind::f16, M = 128,
 // N = 256, K = 16 (128 tensor cycles per instruction, well above the issue
 // cost of an MMA) into two 256-column TMEM accumulators, one per 128-row
 // half.  Warps 4-7 and 8-11: epilogue of the two halves, TMEM -> fp32 global;
@@ -173,8 +173,9 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     tma_load_2d(sB + st * kBBytes + c * kBBox, &tmB, full + st, t.n0 + c * 64, kb * kBK);
             }
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
+        // (the whole warp runs the loop; one elected lane issues)
         const uint64_t da = smem_desc_sw128(smem_u32(sA), 16, 1024);
         // B N-major: 8 k-rows of 128 B per 1024-byte group; the four 64-column
         // boxes are kBBox bytes apart (leading-dimension offset)
@@ -202,13 +203,13 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     const uint64_t das = da + ((uint32_t)(st * kABytes + h * kAHalf) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma_ss(tmem + h * kBN, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)),
+                        umma_ss_w(tmem + h * kBN, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)),
                                 kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     if (kb == p.KB - 1)
-                        umma_commit(acc_full + h);  // this half is final: its epilogue may start
+                        umma_commit_w(acc_full + h);  // this half is final: its epilogue may start
                 }
                 if (ok)
-                    umma_commit(empty + st);
+                    umma_commit_w(empty + st);
             }
         }
         // let the last stage releases land before the CTA exits
