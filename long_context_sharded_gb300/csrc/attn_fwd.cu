@@ -303,6 +303,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             // Descriptors: the address field (bits 0-13, bytes >> 4) of a base
             // descriptor plus a constant offset never carries out of the field
             // (shared memory < 256 KB), so stepping is one add.
+            const uint32_t leader = elect_lane();  // the lane that issues
             const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dk = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t dv = smem_desc_sw128(smem_u32(sV), L::kBoxBytes, 1024);
@@ -314,7 +315,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * L::kBoxBytes + (kk % 4) * 32) >> 4;
-                    umma_ss_w(tmem + col_s(t), da + off, db + off, kIdescQK, kk > 0 ? 1u : 0u);
+                    umma_ss_w(tmem + col_s(t), da + off, db + off, kIdescQK, kk > 0 ? 1u : 0u, leader);
                 }
             };
             // O_t += P_t V over K = 128 keys: P_t from tensor memory (bf16 pairs,
@@ -326,7 +327,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk)
                     umma_ts_w(tmem + col_o(t), tmem + col_s(t) + kk * 8, db + (uint32_t)(kk * (2048 >> 4)),
-                            kIdescPV, (acc_in || kk > 0) ? 1u : 0u);
+                            kIdescPV, (acc_in || kk > 0) ? 1u : 0u, leader);
             };
             int g = 0;                  // tile-iterations of this CTA so far
             int nq = 0;                 // items with work so far (q_full phases)
@@ -355,7 +356,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     if (n == 0) {
                         for (int t = 0; t < ntile; ++t) {
                             issue_qk(t, sk);
-                            umma_commit_w(s_full + t);
+                            umma_commit_w(s_full + t, leader);
                             ++sp[t];
                         }
                     } else {
@@ -381,10 +382,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             issue_pv(t, sv, n > 1);
                             if (n < ntot) {
                                 issue_qk(t, sk);
-                                umma_commit_w(s_full + t);
+                                umma_commit_w(s_full + t, leader);
                                 ++sp[t];
                             } else {
-                                umma_commit_w(o_full + t);
+                                umma_commit_w(o_full + t, leader);
                                 ++od[t];
                             }
                         }

@@ -176,6 +176,7 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         // (the whole warp runs the loop; one elected lane issues)
+        const uint32_t leader = elect_lane();  // the lane that issues
         const uint64_t da = smem_desc_sw128(smem_u32(sA), 16, 1024);
         // B N-major: 8 k-rows of 128 B per 1024-byte group; the four 64-column
         // boxes are kBBox bytes apart (leading-dimension offset)
@@ -204,12 +205,12 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         umma_ss_w(tmem + h * kBN, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)),
-                                kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                                kIdesc, (kb > 0 || kk > 0) ? 1u : 0u, leader);
                     if (kb == p.KB - 1)
-                        umma_commit_w(acc_full + h);  // this half is final: its epilogue may start
+                        umma_commit_w(acc_full + h, leader);  // this half is final: its epilogue may start
                 }
                 if (ok)
-                    umma_commit_w(empty + st);
+                    umma_commit_w(empty + st, leader);
             }
         }
         // let the last stage releases land before the CTA exits

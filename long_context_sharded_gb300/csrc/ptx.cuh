@@ -145,42 +145,53 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 }
 
 // Warp-wide forms of the three calls above: every lane of a converged warp
-// executes them with identical operands and one lane, chosen by elect.sync
-// (the same lane every time), issues the instruction.  Running the issuing
-// loop on a whole warp keeps its descriptors and addresses warp-uniform,
-// which the compiler turns into far cheaper issue code than a one-lane
-// branch gets.
+// executes them with identical operands, and the lane for which `leader` is
+// non-zero (elect_lane(), taken once by the whole warp) issues the
+// instruction.  Running the issuing loop on a whole warp keeps its
+// descriptors and addresses warp-uniform, which the compiler turns into far
+// cheaper issue code than a one-lane branch gets.
+__device__ __forceinline__ uint32_t elect_lane()
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n}\n"
+        : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
+                                          uint32_t accumulate, uint32_t leader)
 {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
         : "memory");
 }
 
 __device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
+                                          uint32_t accumulate, uint32_t leader)
 {
     asm volatile(
         "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
         : "memory");
 }
 
-__device__ __forceinline__ void umma_commit_w(uint64_t *bar)
+__device__ __forceinline__ void umma_commit_w(uint64_t *bar, uint32_t leader)
 {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %1, 0;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n"
-        ::"r"(smem_u32(bar)) : "memory");
+        ::"r"(smem_u32(bar)), "r"(leader) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait()
