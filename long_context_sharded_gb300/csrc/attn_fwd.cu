@@ -55,6 +55,7 @@ struct AttnParams {
     float scale_log2;        // log2(e) / sqrt(d)
     int fault;               // test hook: 1 = drop the first P-ready arrive of tile 0
     int out_bf16;            // fused calls only: O is written as bf16 ([B,Hq,Sq,d], 2 bytes)
+    int out_v8;              // O's base is 32-byte aligned: rows are stored 32 bytes per lane
     float *out;              // fused: out; partial: o_part
     float *lse;              // fused: lse; partial: lse_part
     long long slot_o;        // partial: elements between slots of o_part
@@ -579,28 +580,46 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld_x32(tO + c0, o);
+                // Each lane stores its own row; 32-byte stores (one whole sector
+                // per lane) need half the store instructions and L1 wavefronts
+                // of 16-byte ones, and this loop is bound by them.
                 if (orow && p.out_bf16) {
                     // the row's bf16 elements sit at half the fp32 offset
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        reinterpret_cast<__nv_bfloat16 *>(p.out) + (orow - p.out) + c0);
+                    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + (orow - p.out) + c0;
+                    uint32_t w[16];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t w[4];
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                                  __uint_as_float(o[2 * e + 1]) * inv);
+                        w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                    }
+                    if (p.out_v8) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * c + 2 * e]) * inv,
-                                                                      __uint_as_float(o[8 * c + 2 * e + 1]) * inv);
-                            w[e] = *reinterpret_cast<uint32_t *>(&h2);
-                        }
-                        dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+                        for (int c = 0; c < 2; ++c)
+                            st_global_v8(dst + 16 * c, w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3],
+                                         w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
+                    } else {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                     }
                 } else if (orow) {
-                    float4 *dst = reinterpret_cast<float4 *>(orow + c0);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        dst[c] = make_float4(__uint_as_float(o[4 * c]) * inv, __uint_as_float(o[4 * c + 1]) * inv,
-                                             __uint_as_float(o[4 * c + 2]) * inv,
-                                             __uint_as_float(o[4 * c + 3]) * inv);
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * inv);
+                    if (p.out_v8) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            st_global_v8(orow + c0 + 8 * c, o[8 * c], o[8 * c + 1], o[8 * c + 2], o[8 * c + 3],
+                                         o[8 * c + 4], o[8 * c + 5], o[8 * c + 6], o[8 * c + 7]);
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                                 __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                    }
                 }
             }
             // O_t is read: the next item's first P.V may overwrite it
@@ -735,6 +754,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d));
     p.fault = c.fault;
     p.out_bf16 = c.out_bf16;
+    p.out_v8 = ((uintptr_t)c.out % 32) == 0 ? 1 : 0;
     p.out = c.out;
     p.lse = c.lse;
     p.slot_o = (long long)c.B * c.Hq * c.Sq * c.d;

@@ -287,6 +287,14 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
         : "memory");
 }
 
+// 32-byte global store (eight 32-bit words; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t e, uint32_t f, uint32_t g, uint32_t h)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h) : "memory");
+}
+
 // Packed fp32 pairs (Blackwell f32x2 ALU forms).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
 {
