@@ -72,6 +72,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 2^8
+constexpr float kRescaleFactor = 256.0f;   // 2^kRescaleThreshold
 
 struct Ctl {
     unsigned long long budget;
@@ -485,84 +486,106 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             if (c > lim)
                                 s[c] = -INFINITY;
                     }
-                    // row max: four independent 3-input chains
-                    float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
-                    float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
-#pragma unroll
-                    for (int c = 8; c < 128; c += 8) {
-                        mx0 = max3f(mx0, s[c], s[c + 1]);
-                        mx1 = max3f(mx1, s[c + 2], s[c + 3]);
-                        mx2 = max3f(mx2, s[c + 4], s[c + 5]);
-                        mx3 = max3f(mx3, s[c + 6], s[c + 7]);
-                    }
-                    const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
-                    const float m_cand = fmaxf(m, mx * scale);
-                    const bool need = (m == -INFINITY) ? (m_cand != -INFINITY)
-                                                       : (m_cand - m > kRescaleThreshold);
-                    const float m_new = need ? m_cand : m;
-                    __syncwarp();
-                    if (n > 0 && __any_sync(0xffffffffu, need)) {
-                        const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-                        l *= alpha;
-                        const uint64_t alpha2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t o[32];
-                            tmem_ld_x32(tO + c0, o);
-#pragma unroll
-                            for (int c = 0; c < 32; c += 2) {
-                                uint64_t v2 = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
-                                                     alpha2);
-                                float a, b;
-                                f2_unpack(v2, a, b);
-                                o[c] = __float_as_uint(a);
-                                o[c + 1] = __float_as_uint(b);
-                            }
-                            tmem_st_x32(tO + c0, o);
-                        }
-                    }
-                    m = m_new;
-                    const float mu = (m == -INFINITY) ? 0.f : m;
-                    const uint64_t nmu2 = f2_pack(-mu, -mu);
-                    // p = 2^(s*scale - m): packed FMA, ex2 per element, packed
+                    // p = 2^(s*scale - mu): packed FMA, ex2 per element, packed
                     // partial sums in four chains; bf16 pairs for the P.V MMA are
-                    // stored to tensor memory 16 columns (32 keys) at a time
-                    uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
+                    // stored to tensor memory 16 columns (32 keys) at a time.
+                    // Returns the tile's sum of p.
+                    auto exp_pass = [&](float mu_) -> float {
+                        const uint64_t nmu2 = f2_pack(-mu_, -mu_);
+                        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
 #pragma unroll
-                    for (int cb = 0; cb < 64; cb += 16) {
-                        uint32_t pk[16];
+                        for (int cb = 0; cb < 64; cb += 16) {
+                            uint32_t pk[16];
 #pragma unroll
-                        for (int c = 0; c < 16; c += 4) {
-                            uint64_t pp[4];
+                            for (int c = 0; c < 16; c += 4) {
+                                uint64_t pp[4];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = 2 * (cb + c + u);
-                                const uint64_t x = f2_fma(f2_pack(s[e], s[e + 1]), scale2, nmu2);
-                                float x0, x1;
-                                f2_unpack(x, x0, x1);
-                                const float p0 = ex2_approx(x0);
-                                const float p1 = ex2_approx(x1);
-                                pp[u] = f2_pack(p0, p1);
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);  // low half = p0
-                                pk[c + u] = *reinterpret_cast<uint32_t *>(&h2);
+                                for (int u = 0; u < 4; ++u) {
+                                    const int e = 2 * (cb + c + u);
+                                    const uint64_t x = f2_fma(f2_pack(s[e], s[e + 1]), scale2, nmu2);
+                                    float x0, x1;
+                                    f2_unpack(x, x0, x1);
+                                    const float p0 = ex2_approx(x0);
+                                    const float p1 = ex2_approx(x1);
+                                    pp[u] = f2_pack(p0, p1);
+                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);  // low half = p0
+                                    pk[c + u] = *reinterpret_cast<uint32_t *>(&h2);
+                                }
+                                acc0 = f2_add(acc0, pp[0]);
+                                acc1 = f2_add(acc1, pp[1]);
+                                acc2 = f2_add(acc2, pp[2]);
+                                acc3 = f2_add(acc3, pp[3]);
                             }
-                            acc0 = f2_add(acc0, pp[0]);
-                            acc1 = f2_add(acc1, pp[1]);
-                            acc2 = f2_add(acc2, pp[2]);
-                            acc3 = f2_add(acc3, pp[3]);
+                            tmem_st_x16(tS + cb, pk);
                         }
-                        tmem_st_x16(tS + cb, pk);
+                        float a0, a1, b0, b1, c0, c1, d0, d1;
+                        f2_unpack(acc0, a0, a1);
+                        f2_unpack(acc1, b0, b1);
+                        f2_unpack(acc2, c0, c1);
+                        f2_unpack(acc3, d0, d1);
+                        return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                    };
+                    // The running max m moves only when a tile's max exceeds it by
+                    // more than 2^8.  After the first tile the exponentials are
+                    // taken with the current m straight away: if every p <= 2^8
+                    // (their sum <= 2^8 implies it) m would not have moved and the
+                    // tile is done.  Otherwise (rare) the row max is taken, O and
+                    // l are rescaled if m moves, and the tile is redone -- the
+                    // same arithmetic as taking the max first, without the max on
+                    // the common path.
+                    float tile_l = 0.f;
+                    bool exact = n == 0;
+                    if (!exact) {
+                        tile_l = exp_pass(m == -INFINITY ? 0.f : m);
+                        exact = __any_sync(0xffffffffu, !(tile_l <= kRescaleFactor));
+                        if (exact)
+                            tmem_st_wait();  // the first pass's P stores land before they are replaced
+                    }
+                    if (exact) {
+                        // row max: four independent 3-input chains
+                        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+                        float mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+#pragma unroll
+                        for (int c = 8; c < 128; c += 8) {
+                            mx0 = max3f(mx0, s[c], s[c + 1]);
+                            mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+                            mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+                            mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+                        }
+                        const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
+                        const float m_cand = fmaxf(m, mx * scale);
+                        const bool need = (m == -INFINITY) ? (m_cand != -INFINITY)
+                                                           : (m_cand - m > kRescaleThreshold);
+                        const float m_new = need ? m_cand : m;
+                        __syncwarp();
+                        if (n > 0 && __any_sync(0xffffffffu, need)) {
+                            const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+                            l *= alpha;
+                            const uint64_t alpha2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                            for (int c0 = 0; c0 < D; c0 += 32) {
+                                uint32_t o[32];
+                                tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                                for (int c = 0; c < 32; c += 2) {
+                                    uint64_t v2 = f2_mul(f2_pack(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+                                                         alpha2);
+                                    float a, b;
+                                    f2_unpack(v2, a, b);
+                                    o[c] = __float_as_uint(a);
+                                    o[c + 1] = __float_as_uint(b);
+                                }
+                                tmem_st_x32(tO + c0, o);
+                            }
+                        }
+                        m = m_new;
+                        tile_l = exp_pass(m == -INFINITY ? 0.f : m);
                     }
                     tmem_st_wait();
                     tc_fence_before();
                     if (!(p.fault == 1 && t == 0 && n == 0))
                         mbar_arrive(p_full + t);
-                    float a0, a1, b0, b1, c0, c1, d0, d1;
-                    f2_unpack(acc0, a0, a1);
-                    f2_unpack(acc1, b0, b1);
-                    f2_unpack(acc2, c0, c1);
-                    f2_unpack(acc3, d0, d1);
-                    l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+                    l += tile_l;
                 }
             }
             g += ntot;

@@ -232,6 +232,47 @@ def test_cuda_graph_capture_and_replay(m, cfg):
         assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "graph replay")
 
 
+def _scores_that_jump(B, H, Sq, Skv, d, seed):
+    """Keys in the second half of the sequence score 12x higher: a rank whose
+    shifted order visits a low shard first meets a running max that grows by
+    far more than 2^8 (log2 units) at a later tile."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, Sq, d, generator=g).bfloat16()
+    k = torch.randn(B, H, Skv, d, generator=g)
+    k[:, :, Skv // 2:] *= 12.0
+    v = torch.randn(B, H, Skv, d, generator=g).bfloat16()
+    return q, k.bfloat16(), v
+
+
+def _sum_above_threshold(B, H, Sq, Skv, d, seed):
+    """Every key of the second half scores 2.04 (log2 units) above every key of
+    the first: a later tile's probabilities are all ~4.1 relative to the running
+    max, so their sum passes 2^8 while the max moves by far less than 2^8."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.zeros(B, H, Sq, d)
+    q[..., 0] = 8.0
+    k = torch.zeros(B, H, Skv, d)
+    k[..., 0] = 1.0
+    k[:, :, Skv // 2:, 0] = 3.0
+    v = torch.randn(B, H, Skv, d, generator=g).bfloat16()
+    return q.bfloat16(), k.bfloat16(), v
+
+
+@pytest.mark.parametrize("make", [_scores_that_jump, _sum_above_threshold], ids=["max_jump", "sum_over_2e8"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_paths(m, make, causal):
+    """The softmax takes the exponentials with the running max first and redoes a
+    tile only when its probabilities could exceed 2^8: both redo cases (the max
+    moves, and it does not) must give plain attention, fused and per step."""
+    B, H, Sq, Skv, d, R = 1, 2, 1024, 1024, 128, 4
+    q, k, v = make(B, H, Sq, Skv, d, seed=21)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    out, lse = run_sharded(m, q, k, v, R, 1, causal)
+    assert_close(out, lse, o_ref, l_ref, "fused")
+    _, _, out, lse = run_partial_merge(m, q, k, v, R, 1, causal)
+    assert_close(out, lse, o_ref, l_ref, "partial + merge")
+
+
 def test_shift_orders_agree_on_gpu(m):
     q, k, v = make_qkv(1, 4, 2, 1024, 1024, 128, seed=42)
     o_ref, l_ref = oracle.attn(q, k, v, True)
