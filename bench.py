@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "d784a32097134c58", "bytes_per_launch": 2426705920,
+ATTN_TRAFFIC = {"source_sha": "23f3dbc08e816714", "bytes_per_launch": 2578463744,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
