@@ -4,6 +4,9 @@
 #include <cuda_runtime.h>
 
 #include <limits.h>
+#include <atomic>
+#include <map>
+#include <mutex>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -148,21 +151,24 @@ int finish(int rc, cudaStream_t stream)
 // Number of SMs of the current device (cached per device).
 int sm_count(int *out)
 {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // 0 until looked up
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return fail(MERCURY_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-        *out = cache[dev];
-        return MERCURY_OK;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *out = c;
+            return MERCURY_OK;
+        }
     }
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return fail(MERCURY_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
     if (dev >= 0 && dev < 64)
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     *out = n;
     return MERCURY_OK;
 }
@@ -201,6 +207,7 @@ int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int shi
 // memory is kept for reuse instead of being returned at every synchronise).
 int scratch_pool(cudaMemPool_t *pool)
 {
+    static std::mutex mu;
     static cudaMemPool_t pools[64] = {};
     static bool made[64] = {};
     int dev = 0;
@@ -209,6 +216,7 @@ int scratch_pool(cudaMemPool_t *pool)
         return fail(MERCURY_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64)
         return fail(MERCURY_ECUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);  // first calls from several threads create one pool
     if (!made[dev]) {
         cudaMemPoolProps props = {};
         props.allocType = cudaMemAllocationTypePinned;
@@ -335,6 +343,44 @@ int clear_error()
 int device_sm_count(int *n)
 {
     return sm_count(n);
+}
+
+int prepare_kernel(const void *func, int smem_bytes, KernelInfo *info, char *msg, size_t msg_len)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, KernelInfo> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({func, dev});
+    if (it != done.end()) {
+        *info = it->second;
+        return MERCURY_OK;
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    KernelInfo ki{fa.numRegs, 0};
+    e = cudaDeviceGetAttribute(&ki.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || ki.sms < 1) {
+        snprintf(msg, msg_len, "SM count: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    done[{func, dev}] = ki;
+    *info = ki;
+    return MERCURY_OK;
 }
 
 }  // namespace mercury

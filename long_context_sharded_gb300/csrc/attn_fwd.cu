@@ -665,17 +665,14 @@ using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, vo
 
 EncodeFn get_encode_fn(char *msg, size_t msg_len)
 {
-    static EncodeFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once (thread-safe static initialisation)
+    static const EncodeFn fn = []() -> EncodeFn {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                                          cudaEnableDefault, &q);
-        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = (EncodeFn)ptr;
-    }
+        return (e == cudaSuccess && q == cudaDriverEntryPointSuccess) ? (EncodeFn)ptr : nullptr;
+    }();
     if (!fn)
         snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
     return fn;
@@ -708,47 +705,21 @@ int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &m
 {
     using L = Smem<D, NK, NV>;
     auto kern = attn_fwd_kernel<D, NK, NV>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-        if (e != cudaSuccess) {
-            snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            return MERCURY_ECUDA;
-        }
-        attr_set = true;
-    }
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-        if (e != cudaSuccess) {
-            snprintf(msg, msg_len, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
-            return MERCURY_ECUDA;
-        }
-        launch_regs = fa.numRegs;
-    }
+    KernelInfo ki;
+    int rc = prepare_kernel((const void *)kern, L::kAlloc, &ki, msg, msg_len);
+    if (rc != MERCURY_OK)
+        return rc;
     // setmaxnreg.inc would wait for registers that the launch does not have
-    if (launch_regs < kMinLaunchRegs) {
-        snprintf(msg, msg_len, "kernel built with %d registers/thread, the register split needs %d",
-                 launch_regs, kMinLaunchRegs);
+    if (ki.regs < kMinLaunchRegs) {
+        snprintf(msg, msg_len, "kernel built with %d registers/thread, the register split needs %d", ki.regs,
+                 kMinLaunchRegs);
         return MERCURY_ECUDA;
     }
     if (p.g.n_items > 0x7fffffffLL) {
         snprintf(msg, msg_len, "too many work items (%lld)", p.g.n_items);
         return MERCURY_EINVAL;
     }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess || sms < 1) {
-            snprintf(msg, msg_len, "SM count: %s", cudaGetErrorString(e));
-            sms = 0;
-            return MERCURY_ECUDA;
-        }
-    }
+    const int sms = ki.sms;
     // persistent: one CTA per SM (the shared memory and TMEM use allow one)
     const long long grid = p.g.n_items < sms ? p.g.n_items : sms;
     if (grid < 1)

@@ -276,15 +276,14 @@ using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, vo
 int encode_2d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1, char *msg,
               size_t msg_len)
 {
-    static EncodeFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe static initialisation)
+    static const EncodeFn fn = []() -> EncodeFn {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeFn)ptr;
-    }
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        return (e == cudaSuccess && q == cudaDriverEntryPointSuccess) ? (EncodeFn)ptr : nullptr;
+    }();
     if (!fn) {
         snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
         return MERCURY_ECUDA;
@@ -334,27 +333,11 @@ int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R
         rc = encode_2d(&mb, b, (uint64_t)N, (uint64_t)K, 64, kBK, msg, msg_len);
     if (rc != MERCURY_OK)
         return rc;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_shifted_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGAlloc);
-        if (e != cudaSuccess) {
-            snprintf(msg, msg_len, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            return MERCURY_ECUDA;
-        }
-        attr = true;
-    }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess || sms < 1) {
-            sms = 0;
-            snprintf(msg, msg_len, "SM count: %s", cudaGetErrorString(e));
-            return MERCURY_ECUDA;
-        }
-    }
+    KernelInfo ki;
+    rc = prepare_kernel((const void *)gemm_shifted_kernel, kGAlloc, &ki, msg, msg_len);
+    if (rc != MERCURY_OK)
+        return rc;
+    const int sms = ki.sms;
     const long long grid = p.n_items < sms ? p.n_items : sms;
     if (grid < 1)
         return MERCURY_OK;

@@ -51,6 +51,16 @@ int clear_error();
 // SMs of the current device (cached per device).
 int device_sm_count(int *n);
 
+// Launch preparation of a kernel on the current device, done once per
+// (kernel, device): raises its dynamic shared-memory limit to smem_bytes and
+// reports the registers per thread it was built with and the device's SM
+// count.  Thread-safe.
+struct KernelInfo {
+    int regs;
+    int sms;
+};
+int prepare_kernel(const void *func, int smem_bytes, KernelInfo *info, char *msg, size_t msg_len);
+
 // Run count (1 = fused) with the least estimated time for a call with R
 // virtual ranks each owning a query block, among those whose partials fit in
 // scratch_cap bytes (schedule.cu's cost model, built-in device profile).
