@@ -83,7 +83,7 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
     const long long grid = std::min<long long>(n, p.n_sms);
     std::vector<double> diff(grid + 1, 0.0);
     double everyone = 0.0;
-    // Items sharing (row tile, rank, slot) sit in runs of NHP*Hkv*B
+    // Otherwise items sharing (row tile, rank, slot) sit in runs of NHP*Hkv*B
     // consecutive indices; their cost differs only through the head pair
     // (an odd number of head tiles leaves the last pair with one tile).
     const long long inner = (long long)g.NHP * g.Hkv * g.B;
@@ -105,7 +105,17 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
             diff[b - grid] -= c;
         }
     };
-    for (long long start = 0; start < n; start += inner) {
+    if (g.partial == kFused && !g.causal) {
+        // items of one (batch, KV head) are consecutive: the costs repeat with
+        // period NHP * NRT * Rq
+        const long long period = (long long)g.NHP * g.NRT * g.Rq;
+        std::vector<double> c(period);
+        for (long long j = 0; j < period; ++j)
+            c[j] = item_cost(g, decode_item(g, j), order, p);
+        for (long long i = 0; i < n; ++i)
+            add_range(i, 1, c[i % period]);
+    }
+    for (long long start = 0; start < n && !(g.partial == kFused && !g.causal); start += inner) {
         if (uniform) {
             const Item it = decode_item(g, start);
             add_range(start, std::min(inner, n - start), item_cost(g, it, order, p));

@@ -116,19 +116,31 @@ struct Item {
 };
 
 // Decode work item `idx`.  Fused causal items are ordered heaviest first
-// (longest KV range first) so that a wave of CTAs ends together; items that
-// share a KV head sit next to each other so concurrent CTAs share K/V in L2.
-// Per-step items are ordered by shard first, so CTAs resident together read
-// the same shard; grouped items by run first (neighbouring ranks' runs
-// overlap in shards under the shift).
+// (longest KV range first) so that a wave of CTAs ends together, with the
+// items of one KV head's group next to each other; fused non-causal items
+// (all of equal cost) take one (batch, KV head) at a time, so the CTAs
+// resident together share K/V in L2.  Per-step items are ordered by shard
+// first, so CTAs resident together read the same shard; grouped items by run
+// first (neighbouring ranks' runs overlap in shards under the shift).
 MERCURY_HD Item decode_item(const Geom &g, long long idx)
 {
     Item it;
-    int hp = (int)(idx % g.NHP); idx /= g.NHP;
-    it.hkv = (int)(idx % g.Hkv); idx /= g.Hkv;
-    it.b = (int)(idx % g.B); idx /= g.B;
-    int rt = (int)(idx % g.NRT); idx /= g.NRT;
-    int rank = (int)(idx % g.Rq); idx /= g.Rq;
+    int hp, rt, rank;
+    if (g.partial == kFused && !g.causal) {
+        // equal-cost items: every item of one (batch, KV head) before the next,
+        // so the CTAs resident together read a few heads' K/V from L2
+        hp = (int)(idx % g.NHP); idx /= g.NHP;
+        rt = (int)(idx % g.NRT); idx /= g.NRT;
+        rank = (int)(idx % g.Rq); idx /= g.Rq;
+        it.hkv = (int)(idx % g.Hkv); idx /= g.Hkv;
+        it.b = (int)(idx % g.B); idx /= g.B;
+    } else {
+        hp = (int)(idx % g.NHP); idx /= g.NHP;
+        it.hkv = (int)(idx % g.Hkv); idx /= g.Hkv;
+        it.b = (int)(idx % g.B); idx /= g.B;
+        rt = (int)(idx % g.NRT); idx /= g.NRT;
+        rank = (int)(idx % g.Rq); idx /= g.Rq;
+    }
     it.shard = g.partial != kFused ? (int)idx : -1;
     if (g.causal && g.partial == kFused) {
         rank = g.Rq - 1 - rank;
