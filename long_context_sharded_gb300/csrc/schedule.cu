@@ -105,7 +105,7 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
             diff[b - grid] -= c;
         }
     };
-    if (g.partial == kFused && !g.causal) {
+    if (g.partial == kFused) {
         // items of one (batch, KV head) are consecutive: the costs repeat with
         // period NHP * NRT * Rq
         const long long period = (long long)g.NHP * g.NRT * g.Rq;
@@ -115,7 +115,7 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
         for (long long i = 0; i < n; ++i)
             add_range(i, 1, c[i % period]);
     }
-    for (long long start = 0; start < n && !(g.partial == kFused && !g.causal); start += inner) {
+    for (long long start = 0; start < n && g.partial != kFused; start += inner) {
         if (uniform) {
             const Item it = decode_item(g, start);
             add_range(start, std::min(inner, n - start), item_cost(g, it, order, p));

@@ -126,9 +126,9 @@ MERCURY_HD Item decode_item(const Geom &g, long long idx)
 {
     Item it;
     int hp, rt, rank;
-    if (g.partial == kFused && !g.causal) {
-        // equal-cost items: every item of one (batch, KV head) before the next,
-        // so the CTAs resident together read a few heads' K/V from L2
+    if (g.partial == kFused) {
+        // every item of one (batch, KV head) before the next, so the CTAs
+        // resident together read a few heads' K/V from L2
         hp = (int)(idx % g.NHP); idx /= g.NHP;
         rt = (int)(idx % g.NRT); idx /= g.NRT;
         rank = (int)(idx % g.Rq); idx /= g.Rq;
