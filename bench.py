@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "23f3dbc08e816714", "bytes_per_launch": 2578463744,
+ATTN_TRAFFIC = {"source_sha": "7c01f7ae348b7ab2", "bytes_per_launch": 927411200,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
@@ -98,9 +98,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_sha(*paths: str) -> str:
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# the attention kernel's sources: its traffic record is valid for these bytes
+ATTN_SOURCES = tuple(os.path.join(ROOT, "long_context_sharded_gb300", "csrc", f)
+                     for f in ("attn_fwd.cu", "work.h", "ptx.cuh"))
 
 
 class ClockSampler:
@@ -338,8 +346,8 @@ def run_gpu(args):
     roofline = None
     if not partial:
         achieved = flops / (launch_ms / 1e3) / 1e12
-        src = os.path.join(ROOT, "long_context_sharded_gb300", "csrc", "attn_fwd.cu")
-        traffic = ATTN_TRAFFIC["bytes_per_launch"] if ATTN_TRAFFIC["source_sha"] == source_sha(src) else None
+        traffic = (ATTN_TRAFFIC["bytes_per_launch"] if ATTN_TRAFFIC["source_sha"] == source_sha(*ATTN_SOURCES)
+                   else None)
         roofline = {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,

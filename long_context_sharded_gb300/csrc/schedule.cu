@@ -421,12 +421,12 @@ int mercury_default_cost_profile(int n_sms, mercury_cost_profile *prof)
         return set_error(MERCURY_EINVAL, "n_sms must be >= 1 (got %d)", n_sms);
     // GB300 figures of this library's kernels (mercury_measure_cost_profile
     // on one GB300, SM clock 2.07 GHz).
-    prof->tile_us = 1.47;
+    prof->tile_us = 1.45;
     prof->tile1_us = 1.33;
-    prof->item_us = 9.4;
-    prof->launch_us = 14.7;
-    prof->merge_gbs = 6370.0;
-    prof->hbm_gbs = 6580.0;
+    prof->item_us = 10.2;
+    prof->launch_us = 14.3;
+    prof->merge_gbs = 6320.0;
+    prof->hbm_gbs = 6490.0;
     prof->n_sms = n_sms;
     prof->measured = 0;
     return clear_error();
