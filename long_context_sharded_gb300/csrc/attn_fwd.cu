@@ -8,7 +8,8 @@
 // order[i][j] at step j (the (j+i)%J access of the shift primitive, or its
 // nested two-level form), with the R virtual ranks' data all in local HBM.
 //
-// Per CTA (one work item, up to two 128-row query tiles sharing a KV head):
+// One persistent CTA per SM takes work items in turn (a work item: up to two
+// 128-row query tiles sharing a KV head, one (batch, KV head) at a time):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles into two
 //               shared-memory rings, in the shifted shard order
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane
@@ -18,7 +19,9 @@
 //   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (one query row per
 //               thread): online softmax in the log2 domain, rescaling of O_t
 //               in tensor memory when the running max moves by more than
-//               2^8, bf16 P_t written back over S_t, final O/l and LSE
+//               2^8 (the row max is only taken when a tile's probabilities
+//               could pass that), bf16 P_t written back over S_t, final O/l
+//               and LSE
 // Tensor memory (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+D)
 // O_1 [256+D, 256+2D).
 //
