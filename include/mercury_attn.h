@@ -397,8 +397,9 @@ MERCURY_API int mercury_attn_run_schedule(const void *q, const void *k, const vo
  * fastest.  The choice is cached for the process under (device ordinal, SM
  * count, compute capability, library build, shape, R, shift, budget, top_k).
  * A later call with the same key runs the cached schedule once, timed; if it
- * takes more than 1.5 times its recorded time the entry is dropped and the
- * call tunes again.  On return out / lse hold the attention result (from the
+ * takes more than 1.5 times its recorded time (env MERCURY_TUNE_RECHECK sets
+ * the factor; 0 re-tunes on every call) the entry is dropped and the call
+ * tunes again.  On return out / lse hold the attention result (from the
  * chosen schedule's last run) and *best (if not NULL) the chosen schedule
  * with measured_us set.  *cache_hit (if not NULL) is 1 when no tuning ran.
  * The call synchronises `stream`.

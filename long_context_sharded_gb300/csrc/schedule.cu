@@ -16,6 +16,7 @@
 #include <map>
 #include <mutex>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string>
 #include <vector>
 
@@ -348,6 +349,21 @@ std::map<std::string, mercury_schedule> g_cache;
 
 const char *kBuildId = __DATE__ " " __TIME__;
 
+// A cached schedule is kept while a re-timed run takes at most this factor
+// of its recorded time (1.5; env MERCURY_TUNE_RECHECK overrides, 0 forces a
+// re-tune on every call).
+double recheck_factor()
+{
+    const char *e = getenv("MERCURY_TUNE_RECHECK");
+    if (e && *e) {
+        char *end = nullptr;
+        const double v = strtod(e, &end);
+        if (end && *end == '\0' && v >= 0)
+            return v;
+    }
+    return 1.5;
+}
+
 int cache_key(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int R, int shift, long long budget,
               int top_k, std::string *key)
 {
@@ -584,7 +600,7 @@ int mercury_tune_schedule(const void *q, const void *k, const void *v, int B, in
         double t = 0;
         if ((rc = time_median(runner(cached), 0, 1, s, ev, &t)))
             return rc;
-        if (t <= 1.5 * cached.measured_us) {
+        if (t <= recheck_factor() * cached.measured_us) {
             if ((rc = check_errors_after(s)))
                 return rc;
             if (best)

@@ -303,6 +303,31 @@ def test_output_canaries_untouched(m):
     assert (big_o[n_o:] == 7.25).all() and (big_l[n_l:] == 7.25).all()
 
 
+@pytest.mark.parametrize("bf16", [False, True], ids=["fp32_out", "bf16_out"])
+def test_output_16_byte_aligned_only(m, bf16, monkeypatch):
+    """O at an address that is 16- but not 32-byte aligned takes the 16-byte
+    store path: bit-identical to the 32-byte path, canaries around it intact."""
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "1")
+    B, Hq, Hkv, S, d, R = 1, 4, 2, 512, 128, 4
+    q, k, v = (x.cuda() for x in make_qkv(B, Hq, Hkv, S, S, d, seed=13))
+    dt = torch.bfloat16 if bf16 else torch.float32
+    fn = m.mercury_attn_sharded_bf16 if bf16 else m.mercury_attn_sharded
+    n_o = B * Hq * S * d
+    shift = 16 // torch.tensor([], dtype=dt).element_size()  # 16 bytes
+    big = torch.full((n_o + 2 * shift + 64,), 3.5, dtype=dt, device="cuda")
+    assert big.data_ptr() % 256 == 0
+    out = big[shift:shift + n_o].view(B, Hq, S, d)
+    assert out.data_ptr() % 32 == 16
+    o_ref = torch.empty((B, Hq, S, d), dtype=dt, device="cuda")
+    l_ref = torch.empty((B, Hq, S), device="cuda")
+    lse = torch.empty((B, Hq, S), device="cuda")
+    fn(q, k, v, R, 1, True, out, lse)
+    fn(q, k, v, R, 1, True, o_ref, l_ref)
+    m.mercury_sync_status()
+    assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+    assert (big[:shift] == 3.5).all() and (big[shift + n_o:] == 3.5).all()
+
+
 # ------------------------------------------------------ merge kernel
 
 @pytest.mark.parametrize("n_parts,rows,d", [(1, 7, 128), (4, 33, 64), (64, 1000, 128),

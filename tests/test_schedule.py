@@ -324,6 +324,28 @@ def test_tune_caches_and_rechecks(gpu):
 
 
 @pytest.mark.gpu
+def test_tune_recheck_drops_a_slow_entry(gpu, monkeypatch):
+    """A cached schedule that misses its recorded time by more than the
+    re-check factor is dropped and tuned again (factor 0: always)."""
+    import oracle
+    m = gpu
+    B, Hq, Hkv, Sq, Skv, d, causal, R, shift = 1, 4, 2, 512, 4096, 128, True, 8, 4
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=405)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    m.mercury_tune_cache_clear()
+    _, _, _, hit = m.mercury_tune_schedule(qd, kd, vd, R, shift, causal, 0, 2)
+    assert not hit
+    _, _, _, hit = m.mercury_tune_schedule(qd, kd, vd, R, shift, causal, 0, 2)
+    assert hit
+    monkeypatch.setenv("MERCURY_TUNE_RECHECK", "0")
+    out, lse, best, hit = m.mercury_tune_schedule(qd, kd, vd, R, shift, causal, 0, 2)
+    assert not hit and best.measured_us > 0
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "re-tuned")
+    m.mercury_tune_cache_clear()
+
+
+@pytest.mark.gpu
 def test_measured_profile_is_plausible_and_predicts(gpu):
     import torch
     m = gpu
