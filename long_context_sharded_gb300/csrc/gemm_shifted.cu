@@ -62,6 +62,7 @@ struct GemmParams {
     int KB;            // 64-wide K steps
     long long n_items;
     float *c;
+    int c_v8;          // c is 32-byte aligned (N % 8 == 0 keeps every row so)
     unsigned long long wait_ns;
     unsigned char order[kMaxR * kMaxR];
 };
@@ -241,7 +242,14 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                 uint32_t v[32];
                 tmem_ld_x32(tmem + lane_field + acc * kBN + c0, v);
                 if (row_ok) {
-                    if (c0 + 32 <= n_lim) {
+                    if (c0 + 32 <= n_lim && p.c_v8) {
+                        // 32 bytes per lane: half the store instructions and L1
+                        // wavefronts of 16-byte stores
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            st_global_v8(crow + c0 + 8 * q, v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3],
+                                         v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]);
+                    } else if (c0 + 32 <= n_lim) {
                         float4 *dst = reinterpret_cast<float4 *>(crow + c0);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -320,6 +328,7 @@ int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R
     p.KB = (K + kBK - 1) / kBK;
     p.n_items = (long long)R * R * p.RT * p.CT;
     p.c = c;
+    p.c_v8 = ((uintptr_t)c % 32 == 0 && N % 8 == 0) ? 1 : 0;
     p.wait_ns = wait_ns;
     for (int i = 0; i < R * R; ++i)
         p.order[i] = (unsigned char)order[i];
