@@ -359,7 +359,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         tc_fence_after();
                     }
                     if (n == 0) {
-                        for (int t = 0; t < ntile; ++t) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (t >= ntile)
+                                break;
                             issue_qk(t, sk);
                             umma_commit_w(s_full + t, leader);
                             ++sp[t];
@@ -371,7 +374,11 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             ok = false;
                             break;
                         }
-                        for (int t = 0; t < ntile && ok; ++t) {
+                        // t unrolled: sp[] and od[] stay in registers
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (t >= ntile || !ok)
+                                break;
                             if (!wait_phase(p_full + t, (sp[t] - 1) & 1, ctl, 0x203)) {
                                 ok = false;
                                 break;
