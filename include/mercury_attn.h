@@ -95,11 +95,13 @@ MERCURY_API int mercury_plan_shift(int R, int shift, int *order);
  * Schedule: when one work item per rank's whole step sequence would leave the
  * GPU short of work (short query side, long KV), each rank's step sequence is
  * cut into g runs of consecutive steps; each run's partial (O, LSE) goes to
- * scratch memory and the runs are merged as by mercury_lse_merge.  The
- * scratch, g * B*Hq*Sq*(d+1)*4 bytes (at most 4 GiB, env
- * MERCURY_SCRATCH_MAX_BYTES), comes stream-ordered from a memory pool the
- * library keeps per device; env MERCURY_SPLIT_GROUPS=g forces g runs (1: no
- * split).  The result is the same up to rounding.
+ * scratch memory and the runs are merged as by mercury_lse_merge.  g is the
+ * run count that mercury_plan_schedules' cost model (built-in profile, this
+ * R, Rq = R) predicts fastest among those whose scratch,
+ * g * B*Hq*Sq*(d+1)*4 bytes, fits in 4 GiB (env MERCURY_SCRATCH_MAX_BYTES);
+ * the scratch comes stream-ordered from a memory pool the library keeps per
+ * device; env MERCURY_SPLIT_GROUPS=g forces g runs (1: no split).  The result
+ * is the same up to rounding.
  * Requirements: B, Hq, Hkv, Sq, Skv >= 1; Hq % Hkv == 0; d in {64, 128};
  * 1 <= R <= MERCURY_MAX_R; Sq % R == 0 and Skv % R == 0; causal requires
  * Sq <= Skv; valid shift (as in mercury_plan_shift); every element count fits
