@@ -294,7 +294,7 @@ def run_gpu(args):
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_cmp = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
-        e_steps = max(3, min(args.steps, 20))
+        e_steps = max(3, min(args.steps, 50))
 
         def e2e_step(i):
             dq_, dk_, dv_, do_, dl_, oh, lh = slots[i % 2]
