@@ -117,7 +117,9 @@ MERCURY_API int mercury_attn_sharded(const void *q, const void *k, const void *v
 /*
  * mercury_attn_sharded_bf16 -- mercury_attn_sharded with O written as bf16
  * (out [B,Hq,Sq,d] bf16, 16-byte aligned; lse stays fp32), halving the output
- * footprint.  Always the fused schedule (no split-KV scratch).  Arguments,
+ * footprint.  Same schedule choice as mercury_attn_sharded; when it splits,
+ * the partials stay fp32 in scratch and the merged O is rounded to bf16, so
+ * the result is the fp32 call's O rounded to nearest.  Arguments,
  * requirements and errors as mercury_attn_sharded.
  */
 MERCURY_API int mercury_attn_sharded_bf16(const void *q, const void *k, const void *v,

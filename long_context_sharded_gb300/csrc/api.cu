@@ -237,14 +237,17 @@ int scratch_pool(cudaMemPool_t *pool)
 
 // Run a validated call that produces the final O and LSE: the fused
 // schedule writes them directly; a split schedule (per-step or grouped)
-// writes one partial per slot into pooled scratch and merges the slots.
-int run_to_output(AttnCall &c, float *out, float *lse, cudaStream_t s)
+// writes one fp32 partial per slot into pooled scratch and merges the slots.
+// out_bf16: out holds bf16 elements.
+int run_to_output(AttnCall &c, float *out, float *lse, cudaStream_t s, int out_bf16 = 0)
 {
     if (c.mode == kFused) {
         c.out = out;
         c.lse = lse;
+        c.out_bf16 = out_bf16;
         return launch_attention(c, s, g_msg, sizeof g_msg);
     }
+    c.out_bf16 = 0;  // the partials stay fp32
     Geom g;
     if (make_geom(g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups, c.Rq))
         return fail(MERCURY_EINVAL, "unsupported shape");
@@ -266,7 +269,8 @@ int run_to_output(AttnCall &c, float *out, float *lse, cudaStream_t s)
     c.lse = l_part;
     rc = launch_attention(c, s, g_msg, sizeof g_msg);
     if (rc == MERCURY_OK)
-        rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, c.d, out, lse, s, g_msg, sizeof g_msg);
+        rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, c.d, out, lse, s, g_msg, sizeof g_msg,
+                              out_bf16);
     e = cudaFreeAsync(scratch, s);
     if (rc == MERCURY_OK && e != cudaSuccess)
         rc = fail(MERCURY_ECUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
@@ -274,7 +278,8 @@ int run_to_output(AttnCall &c, float *out, float *lse, cudaStream_t s)
 }
 
 int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
-                int d, int R, int shift, int causal, float *out, float *lse, void *stream, int partial)
+                int d, int R, int shift, int causal, float *out, float *lse, void *stream, int partial,
+                int out_bf16 = 0)
 {
     int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, out, lse, partial);
     if (rc)
@@ -317,7 +322,7 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
         c.lse = lse;
         rc = launch_attention(c, s, g_msg, sizeof g_msg);
     } else {
-        rc = run_to_output(c, out, lse, s);
+        rc = run_to_output(c, out, lse, s, out_bf16);
     }
     return finish(rc, s);
 }
@@ -447,36 +452,7 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
 int mercury_attn_sharded_bf16(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq,
                               int Skv, int d, int R, int shift, int causal, void *out, float *lse, void *stream)
 {
-    int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, (const float *)out, lse, 0);
-    if (rc)
-        return rc;
-    int order[kMaxR * kMaxR];
-    if (plan_shift(R, shift, order))
-        return fail(MERCURY_EINVAL, "invalid (R, shift)");
-    AttnCall c;
-    c.q = q;
-    c.k = k;
-    c.v = v;
-    c.B = B;
-    c.Hq = Hq;
-    c.Hkv = Hkv;
-    c.Sq = Sq;
-    c.Skv = Skv;
-    c.d = d;
-    c.R = R;
-    c.Rq = R;
-    c.causal = causal ? 1 : 0;
-    c.mode = kFused;
-    c.n_groups = 1;
-    c.order = order;
-    c.out = (float *)out;
-    c.lse = lse;
-    c.out_bf16 = 1;
-    c.wait_ns = wait_budget_ns();
-    c.fault = fault_mode();
-    cudaStream_t s = (cudaStream_t)stream;
-    rc = launch_attention(c, s, g_msg, sizeof g_msg);
-    return finish(rc, s);
+    return attn_common(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, (float *)out, lse, stream, 0, 1);
 }
 
 int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,

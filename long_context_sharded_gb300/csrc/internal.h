@@ -23,8 +23,9 @@ struct AttnCall {
 
 int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len);
 
+// out_bf16: out holds bf16 elements (the merged fp32 values rounded to nearest).
 int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
-                     float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len);
+                     float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len, int out_bf16 = 0);
 
 // The split-KV schedule with its partials in the library's fixed-size
 // device array instead of allocated scratch (noalloc.cu).

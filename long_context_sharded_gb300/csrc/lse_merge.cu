@@ -12,8 +12,10 @@
 // TPR*VEC*16-byte read.  The LSE values of a row are spread over the group's
 // lanes, reduced with warp shuffles, and the weights broadcast back by
 // shuffle.  Parts with LSE = -inf have weight 0 and are not read.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdint.h>
 #include <stdio.h>
 
 #include "internal.h"
@@ -26,7 +28,7 @@ constexpr int kMergeThreads = 256;
 template <int TPR, int VEC>
 __global__ void __launch_bounds__(kMergeThreads)
 lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, int n_parts,
-                 long long rows, int d, float *__restrict__ out, float *__restrict__ lse)
+                 long long rows, int d, float *__restrict__ out, float *__restrict__ lse, int out_bf16)
 {
     constexpr int kRowsPerWarp = 32 / TPR;
     const int lane = threadIdx.x % 32;
@@ -88,7 +90,19 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
             }
         }
     }
-    if (active) {
+    if (active && out_bf16) {
+        // out holds bf16: four elements (8 bytes) per float4 of the row
+        uint2 *dst = reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + row * (long long)d);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            const int c = g + v * TPR;
+            if (c < nvec) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v].x, acc[v].y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v].z, acc[v].w);
+                dst[c] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            }
+        }
+    } else if (active) {
         float4 *dst = reinterpret_cast<float4 *>(out + row * (long long)d);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
@@ -96,6 +110,8 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
             if (c < nvec)
                 dst[c] = acc[v];
         }
+    }
+    if (active) {
         if (g == 0)
             lse[row] = L;
     }
@@ -103,7 +119,7 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
 
 template <int TPR, int VEC>
 int launch(const float *o_part, const float *lse_part, int n_parts, long long rows, int d, float *out,
-           float *lse, cudaStream_t stream, char *msg, size_t msg_len)
+           float *lse, cudaStream_t stream, char *msg, size_t msg_len, int out_bf16)
 {
     constexpr int kRowsPerBlock = (kMergeThreads / 32) * (32 / TPR);
     const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
@@ -112,7 +128,7 @@ int launch(const float *o_part, const float *lse_part, int n_parts, long long ro
         return MERCURY_EINVAL;
     }
     lse_merge_kernel<TPR, VEC><<<(unsigned)blocks, kMergeThreads, 0, stream>>>(o_part, lse_part, n_parts,
-                                                                               rows, d, out, lse);
+                                                                               rows, d, out, lse, out_bf16);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "merge kernel launch: %s", cudaGetErrorString(e));
@@ -124,25 +140,25 @@ int launch(const float *o_part, const float *lse_part, int n_parts, long long ro
 }  // namespace
 
 int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
-                     float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len)
+                     float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len, int out_bf16)
 {
     if (rows == 0)
         return MERCURY_OK;
     const int nvec = d / 4;
     if (nvec <= 4)
-        return launch<4, 1>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
+        return launch<4, 1>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
     if (nvec <= 8)
-        return launch<8, 1>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
+        return launch<8, 1>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
     // d = 64 and 128: half a warp per row, two float4 per lane per part (more
     // rows and more loads in flight per warp measured 3-5 % faster than a
     // whole warp per row with one float4 per lane)
     if (nvec <= 16)
-        return launch<8, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
+        return launch<8, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
     if (nvec <= 32)
-        return launch<16, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
+        return launch<16, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
     if (nvec <= 64)
-        return launch<32, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
-    return launch<32, 4>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len);
+        return launch<32, 2>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
+    return launch<32, 4>(o_part, lse_part, n_parts, rows, d, out, lse, stream, msg, msg_len, out_bf16);
 }
 
 }  // namespace mercury

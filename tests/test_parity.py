@@ -182,11 +182,12 @@ def test_decode_matches_oracle(m, cfg):
 
 @pytest.mark.parametrize("cfg", [(1, 4, 4, 512, 512, 64, 4, 1, False), (1, 8, 2, 1024, 1024, 128, 8, 4, True),
                                  (1, 8, 1, 128, 4096, 128, 4, 1, False)], ids=lambda c: "x".join(map(str, c)))
-def test_sharded_bf16_output(m, cfg, monkeypatch):
+@pytest.mark.parametrize("groups", [1, 4], ids=["fused", "split4"])
+def test_sharded_bf16_output(m, cfg, groups, monkeypatch):
     """bf16 O: within the parity tolerance of the oracle, and equal to the fp32
-    fused path's O rounded to bf16 (the fp32 call is held to the fused
-    schedule: a split would round differently)."""
-    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "1")
+    call's O rounded to bf16 under the same schedule (fused, or cut into runs
+    whose fp32 partials are merged before the rounding)."""
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", str(groups))
     B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
     q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 99)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
