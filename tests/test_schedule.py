@@ -355,8 +355,9 @@ def test_measured_profile_is_plausible_and_predicts(gpu):
     assert 0.2 < prof.tile_us < 20 and 0 < prof.tile1_us <= prof.tile_us * 1.2
     assert 0 <= prof.item_us < 100 and 0 <= prof.launch_us < 200
     assert 500 < prof.merge_gbs < 20000 and 500 < prof.hbm_gbs < 20000
-    # the estimate of a causal GQA call is within 30 % of its measured time
-    B, Hq, Hkv, Sq, Skv, d, causal, R, shift = 1, 32, 8, 8192, 8192, 128, True, 8, 1
+    # the estimate of a long causal GQA call (the bench shape) is within 30 % of
+    # its measured time
+    B, Hq, Hkv, Sq, Skv, d, causal, R, shift = 1, 32, 8, 32768, 32768, 128, True, 8, 1
     plans, _ = m.mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, 0, prof, 1)
     q, k, v = (x.cuda() for x in make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=9))
     out = torch.empty((B, Hq, Sq, d), device="cuda")
