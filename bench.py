@@ -5,20 +5,24 @@
     python bench.py --impl reference ...      # the fp64 CPU oracle, timed
 
 One step = one pass of the hot path over one batch of synthetic input: a
-mercury_attn_sharded call on the Llama-3-8B-like GQA workload (B 1, 32 query /
-8 KV heads, d 128, 32K tokens, causal, R = 8 virtual ranks, flat shift): it
-shards Q and K/V, walks the shards in the shifted order, skips causally masked
-shards, runs the tcgen05 attention patch and finalises O and LSE (the
-per-step partials are combined on the fly, i.e. the log-sum-exp merge is
-fused).  The separate partial + merge path is measured as a secondary figure
-on the 2M-token MQA chunk (mercury_attn_partial + mercury_lse_merge), which is
-where the merge's HBM bandwidth is reported.
+mercury_attn_sharded call on the largest single-GPU workload, the
+Llama-3-70B-like GQA prefill (B 1, 64 query / 8 KV heads, d 128, 128K tokens,
+causal, R = 8 virtual ranks in the nested 2 x 4 shift order): it shards Q and
+K/V, walks the shards in the shifted order, skips causally masked shards, runs
+the tcgen05 attention patch and finalises O and LSE (the per-step partials are
+combined on the fly, i.e. the log-sum-exp merge is fused).
+
+The line's "configs" object times every workload on its own (CUDA events,
+median of a short burst): the small MHA case, the 32K GQA causal prefill, the
+batch-16 4K MHA, the headline itself, and the 2M-token MQA chunk through the
+per-step partials and the separate merge, where the merge's HBM bandwidth is
+reported.
 
 Metric: attention TFLOP/s = 4 * d * (unmasked query/key pairs) * B * Hq per
-step / time.  Inputs (384 MiB) are larger than L2, so no flush is needed
-between steps.  Several GPUs (torchrun) run independent replicas: the path
-needs no exchange on one GPU per replica, so value = sum of all ranks' work /
-max-over-ranks time ("weak" scaling).
+step / time.  Inputs (2.5 GiB on the headline) are larger than L2, so no flush
+is needed between steps.  Several GPUs (torchrun) run independent replicas:
+the path needs no exchange on one GPU per replica, so value = sum of all
+ranks' work / max-over-ranks time ("weak" scaling).
 """
 from __future__ import annotations
 
@@ -40,14 +44,15 @@ from long_context_sharded_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, atte
 
 METRIC = "attention TFLOP/s (bf16 fwd, 1×GB300) and % of dense BF16 peak; merge HBM GB/s"
 UNIT = "TFLOP/s"
-MERGE_WORKLOAD = "mqa_b1_hq8_hkv1_d128_sq2k_skv2m_r64_merge"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of one attention launch from an ncu capture (profiles/), valid
-# only for the kernel source it was taken on (sha256 of attn_fwd.cu, first 16
-# hex digits).  Reported as null once the kernel has changed.
-ATTN_TRAFFIC = {"source_sha": "f5bee2595a63049d", "bytes_per_launch": 925422592,
-                "profile": "profiles/attn_fwd_gqa32k_causal_full.md"}
+# DRAM traffic of one attention launch per workload, from an ncu capture,
+# valid only for the kernel source it was taken on (sha256 of the attention
+# kernel's sources, first 16 hex digits).  Reported as null once the kernel
+# has changed or when no capture of that workload exists.
+ATTN_TRAFFIC = {
+    "gqa_b1_hq32_hkv8_d128_s32k_causal_r8": {"source_sha": "f5bee2595a63049d", "bytes_per_launch": 925422592},
+}
 
 
 # ------------------------------------------------------------------ helpers
@@ -109,6 +114,14 @@ def source_sha(*paths: str) -> str:
 # the attention kernel's sources: its traffic record is valid for these bytes
 ATTN_SOURCES = tuple(os.path.join(ROOT, "long_context_sharded_gb300", "csrc", f)
                      for f in ("attn_fwd.cu", "work.h", "ptx.cuh"))
+
+
+def attn_traffic(workload: str):
+    """Recorded DRAM bytes of one attention launch on `workload`, or None."""
+    rec = ATTN_TRAFFIC.get(workload)
+    if rec and rec["source_sha"] == source_sha(*ATTN_SOURCES):
+        return rec["bytes_per_launch"]
+    return None
 
 
 class ClockSampler:
@@ -214,6 +227,106 @@ def cpu_cores() -> int:
 
 # --------------------------------------------------------------- GPU arm
 
+# Dense bf16 tensor-core work of one SM per clock: an M = 128, N = 128, K = 16
+# kind::f16 MMA (524,288 FLOP) takes 64 cycles on a GB300 SM when issued back
+# to back.  Times the SM count and the sampled SM clock, this is the tensor
+# pipe's ceiling at the clock the kernel actually ran at.
+TENSOR_FLOP_PER_CYCLE_PER_SM = 8192
+
+
+def device_qkv(w, dev):
+    from long_context_sharded_gb300.inputs import make_qkv
+    q, k, v = make_qkv(w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], seed=w["seed"], scale=w["scale"])
+    return q, k, v, q.to(dev), k.to(dev), v.to(dev)
+
+
+def launches_per_call(m, w, n_sms: int) -> int:
+    """Kernels one mercury_attn_sharded call launches: 1 for the fused
+    schedule, 2 when the library's chooser splits it (attention + merge).  The
+    chooser takes the fastest predicted run count with Rq = R whose scratch
+    fits in 4 GiB; the same planner gives the same answer here."""
+    prof = m.mercury_default_cost_profile(n_sms)
+    plans, _ = m.mercury_plan_schedules(w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], w["causal"],
+                                        w["R"], w["shift"], 0, prof, 512)
+    cap = int(os.environ.get("MERCURY_SCRATCH_MAX_BYTES", str(4 << 30)))
+    forced = int(os.environ.get("MERCURY_SPLIT_GROUPS", "0") or 0)
+    if forced >= 1:
+        return 1 if forced == 1 or w["R"] == 1 else 2
+    for p in plans:
+        if p.Rq == w["R"] and p.scratch_bytes <= cap:
+            return 1 if p.n_runs == 1 else 2
+    return 1
+
+
+def clock_peak_tflops(n_sms: int, sm_mhz):
+    if not sm_mhz:
+        return None
+    return TENSOR_FLOP_PER_CYCLE_PER_SM * n_sms * sm_mhz * 1e6 / 1e12
+
+
+def time_calls(fn, stream, reps: int, warmup: int = 3):
+    """CUDA-event time of each of `reps` calls of fn on `stream` (ms)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(reps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+
+
+def measure_config(m, name, dev, stream, peaks, n_sms, reps):
+    """One workload, timed on its own: the fused call (mercury_attn_sharded),
+    or for the partial-mode workload the per-step partials and the merge
+    separately plus the same chunk through mercury_attn_sharded's own
+    schedule.  Each figure is the median of `reps` back-to-back calls (CUDA
+    events on the launching stream); a short burst, so fractions are of the
+    burst peak."""
+    import torch
+    w = dict(WORKLOADS[name], name=name)
+    B, Hq, Sq, d, R = w["B"], w["Hq"], w["Sq"], w["d"], w["R"]
+    _, _, _, qd, kd, vd = device_qkv(w, dev)
+    flops = attention_flops(w)
+    out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
+    burst = peaks["bf16_tflops"]
+    res = {"mode": "fused" if w["mode"] == "fused" else "partial+merge", "reps": reps, "flop": flops}
+    if w["mode"] == "fused":
+        ms = statistics.median(time_calls(
+            lambda: m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream), stream, reps))
+        tf = flops / (ms / 1e3) / 1e12
+        res.update({"ms": round(ms, 4), "tflops": round(tf, 2), "frac": round(tf / burst, 4),
+                    "launches_per_call": launches_per_call(m, w, n_sms)})
+    else:
+        op = torch.empty((R, B, Hq, Sq, d), dtype=torch.float32, device=dev)
+        lp = torch.empty((R, B, Hq, Sq), dtype=torch.float32, device=dev)
+        tp = statistics.median(time_calls(
+            lambda: m.mercury_attn_partial(qd, kd, vd, R, w["shift"], w["causal"], op, lp, stream), stream, reps))
+        tm = statistics.median(time_calls(lambda: m.mercury_lse_merge(op, lp, out, lse, stream), stream, reps))
+        ts = statistics.median(time_calls(
+            lambda: m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream), stream, reps))
+        rows = B * Hq * Sq
+        merge_bytes = (R + 1) * rows * (4 * d + 4)
+        gbs = merge_bytes / (tm / 1e3) / 1e9
+        res.update({"partial_ms": round(tp, 4), "attention_tflops": round(flops / (tp / 1e3) / 1e12, 2),
+                    "attention_frac": round(flops / (tp / 1e3) / 1e12 / burst, 4),
+                    "merge_ms": round(tm, 4), "merge_bytes": merge_bytes, "merge_gbs": round(gbs, 1),
+                    "merge_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "ms": round(tp + tm, 4), "tflops": round(flops / ((tp + tm) / 1e3) / 1e12, 2),
+                    "frac": round(flops / ((tp + tm) / 1e3) / 1e12 / burst, 4),
+                    "sharded_auto_ms": round(ts, 4),
+                    "sharded_auto_tflops": round(flops / (ts / 1e3) / 1e12, 2)})
+        del op, lp
+    m.mercury_sync_status(stream)
+    del qd, kd, vd, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import torch
 
@@ -222,15 +335,14 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
     from long_context_sharded_gb300 import mercury as m
-    from long_context_sharded_gb300.inputs import make_qkv
 
     w = dict(WORKLOADS[args.workload], name=args.workload)
     B, Hq, Hkv, Sq, Skv, d = w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"]
     R, shift, causal = w["R"], w["shift"], w["causal"]
     partial = w["mode"] == "partial"
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     flops = attention_flops(w)
-    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=w["seed"], scale=w["scale"])
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    q, k, v, qd, kd, vd = device_qkv(w, dev)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
@@ -246,13 +358,14 @@ def run_gpu(args):
         else:
             m.mercury_attn_sharded(qd, kd, vd, R, shift, causal, out, lse, stream)
 
-    launches_per_step = 2 if partial else 1
+    launches_per_step = 2 if partial else launches_per_call(m, w, n_sms)
     for _ in range(args.warmup):
         step()
     m.mercury_sync_status(stream)
 
     sampler = ClockSampler(local)
-    if rank == 0 and not args.no_clocks:
+    sampling = rank == 0 and not args.no_clocks
+    if sampling:
         sampler.start()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier(world)
@@ -265,18 +378,19 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier(world)
-    rows = sampler.stop() if rank == 0 and not args.no_clocks else []
     m.mercury_sync_status(stream)
     per_step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     elapsed_s = ev[0].elapsed_time(ev[args.steps]) / 1e3
     max_s = max_over_ranks(elapsed_s, world, dev)
     value = aggregate_value(flops, args.steps, world, max_s) / 1e12
 
-    # end to end through the public API with host buffers: every step copies
+    # End to end through the public API with host buffers: every step copies
     # its inputs from pinned host memory to the device, runs the call and
     # copies O and LSE back.  Steps are pipelined the way a caller streaming
     # batches would: two device buffer slots, H2D on one stream, compute on
     # another, D2H on a third, so step i's copies overlap step i-1's compute.
+    # The copies' own durations (CUDA events on the copy streams) give the
+    # host-link rates the pipeline saw.
     e2e = None
     if not args.no_e2e:
         qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -294,16 +408,20 @@ def run_gpu(args):
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_cmp = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
-        e_steps = max(3, min(args.steps, 50))
+        e_steps = max(3, min(args.steps, 20))
+        copy_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e_steps + 2)]
 
         def e2e_step(i):
             dq_, dk_, dv_, do_, dl_, oh, lh = slots[i % 2]
+            ce = copy_ev[i]
             with torch.cuda.stream(s_in):
                 if i >= 2:
                     s_in.wait_event(ev_cmp[i % 2])      # slot's inputs no longer read
+                ce[0].record(s_in)
                 dq_.copy_(qh, non_blocking=True)
                 dk_.copy_(kh, non_blocking=True)
                 dv_.copy_(vh, non_blocking=True)
+                ce[1].record(s_in)
                 ev_in[i % 2].record(s_in)
             with torch.cuda.stream(s_cmp):
                 s_cmp.wait_event(ev_in[i % 2])
@@ -317,12 +435,14 @@ def run_gpu(args):
                 ev_cmp[i % 2].record(s_cmp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_cmp[i % 2])
+                ce[2].record(s_out)
                 oh.copy_(do_, non_blocking=True)
                 lh.copy_(dl_, non_blocking=True)
+                ce[3].record(s_out)
                 ev_out[i % 2].record(s_out)
 
         for i in range(2):
-            e2e_step(i)
+            e2e_step(e_steps + i)
         torch.cuda.synchronize(dev)
         barrier(world)
         t0 = time.perf_counter()
@@ -335,47 +455,72 @@ def run_gpu(args):
         e_s = max_over_ranks(e_wall, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
         d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+        h2d_ms = statistics.mean(copy_ev[i][0].elapsed_time(copy_ev[i][1]) for i in range(e_steps))
+        d2h_ms = statistics.mean(copy_ev[i][2].elapsed_time(copy_ev[i][3]) for i in range(e_steps))
         e2e = {"value": round(aggregate_value(flops, e_steps, world, e_s) / 1e12, 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
-               "timing": "host wall clock around the steps, all streams synchronised at both ends",
+               "h2d_gbs": round(h2d / (h2d_ms / 1e3) / 1e9, 1), "d2h_gbs": round(d2h / (d2h_ms / 1e3) / 1e9, 1),
+               "h2d_ms": round(h2d_ms, 3), "d2h_ms": round(d2h_ms, 3),
+               "timing": "host wall clock around the steps, all streams synchronised at both ends; "
+                         "copy rates from CUDA events around each step's copies",
                "pipelining": "2 buffer slots; H2D, compute and D2H on three streams"}
         del qh, kh, vh, slots
 
     peaks, peak_kind = load_peaks()
-    launch_ms = statistics.mean(per_step_ms) if not partial else None
-    roofline = None
-    if not partial:
-        achieved = flops / (launch_ms / 1e3) / 1e12
-        traffic = (ATTN_TRAFFIC["bytes_per_launch"] if ATTN_TRAFFIC["source_sha"] == source_sha(*ATTN_SOURCES)
-                   else None)
-        roofline = {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": round(achieved, 2),
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
-                    "peak_kind": "%s burst bf16 (cuBLAS)" % peak_kind,
-                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
-                    "algorithmic_flop_per_launch": flops,
-                    "algorithmic_bytes_per_launch": (q.numel() + k.numel() + v.numel()) * 2
-                    + out.numel() * 4 + lse.numel() * 4}
+    t_cfg0 = time.time()
+    configs = None
+    if not args.no_configs and rank == 0 and world == 1:
+        configs = {"peak": peaks["bf16_tflops"],
+                   "peak_kind": "%s burst bf16 (cuBLAS): each figure is a short burst of calls" % peak_kind}
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            reps = 100 if attention_flops(WORKLOADS[name]) < 1e10 else 10
+            configs[name] = measure_config(m, name, dev, stream, peaks, n_sms, reps)
+    t_cfg1 = time.time()
+    rows = sampler.stop() if sampling else []
+    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1) if rows else None
+    clocks_cfg = ClockSampler.summarise(rows, t_cfg0, t_cfg1) if rows and configs else None
 
-    secondary = None
-    if not args.no_secondary and rank == 0 and world == 1:
-        secondary = measure_merge_path(m, dev, stream, peaks, peak_kind)
+    launch_ms = statistics.mean(per_step_ms)
+    achieved = flops / (launch_ms / 1e3) / 1e12
+    # A timed region of seconds of back-to-back tensor work runs under the
+    # power cap: its fraction is of the sustained peak; a short one of the
+    # burst peak.  Either way the clock-normalised fraction (achieved over the
+    # tensor pipe's ceiling at the sampled median SM clock) is given too.
+    long_region = elapsed_s > 1.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    cp = clock_peak_tflops(n_sms, clocks["sm_mhz"] if clocks else None)
+    roofline = {"kernel": "attn_fwd_kernel" + (" + lse_merge_kernel" if launches_per_step > 1 else ""),
+                "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": attn_traffic(args.workload),
+                "peak_kind": "%s %s bf16 (cuBLAS); timed region %.2f s of back-to-back launches" % (
+                    peak_kind, "sustained" if long_region else "burst", elapsed_s),
+                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "clock_peak": None if cp is None else {
+                    "tflops": round(cp, 1), "sm_mhz": clocks["sm_mhz"], "frac": round(achieved / cp, 4),
+                    "basis": "%d FLOP/cycle/SM x %d SMs x median SM clock in the timed region" % (
+                        TENSOR_FLOP_PER_CYCLE_PER_SM, n_sms)},
+                "algorithmic_flop_per_launch": flops,
+                "algorithmic_bytes_per_launch": (q.numel() + k.numel() + v.numel()) * 2
+                + out.numel() * 4 + lse.numel() * 4}
+    if configs is not None:
+        headline = {"mode": "fused" if not partial else "partial+merge", "ms": round(statistics.median(per_step_ms), 4),
+                    "tflops": round(achieved, 2), "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "flop": flops, "source": "the headline timed region (%d steps)" % args.steps,
+                    "launches_per_call": launches_per_step}
+        configs = dict([(k_, v_) for k_, v_ in configs.items() if k_ in ("peak", "peak_kind")]
+                       + [(n, headline if n == args.workload else configs[n]) for n in WORKLOADS])
+        configs["clocks"] = clocks_cfg
         torch.cuda.empty_cache()
-        # the schedule planner's estimates (built-in profile) beside the
-        # measured times of the same schedules
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        prof = m.mercury_default_cost_profile(sms)
+        # the schedule planner's estimate (built-in profile) beside the measured time
+        prof = m.mercury_default_cost_profile(n_sms)
         top = m.mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, 0, prof, 1)[0][0]
-        cw = WORKLOADS[MERGE_WORKLOAD]
-        ctop = m.mercury_plan_schedules(cw["B"], cw["Hq"], cw["Hkv"], cw["Sq"], cw["Skv"], cw["d"], cw["causal"],
-                                        cw["R"], cw["shift"], 0, prof, 1)[0][0]
-        secondary["schedule_model"] = {
-            "bench_workload": {"schedule": [top.R, top.Rq, top.n_runs], "predicted_ms": round(top.predicted_us / 1e3, 4),
-                               "measured_ms": round(statistics.median(per_step_ms), 4)},
-            "merge_workload": {"schedule": [ctop.R, ctop.Rq, ctop.n_runs],
-                               "predicted_ms": round(ctop.predicted_us / 1e3, 4),
-                               "measured_ms_sharded_auto": secondary["sharded_auto_ms"]},
-            "schedule_keys": ["R", "Rq", "n_runs"]}
+        configs["schedule_model"] = {"workload": args.workload, "schedule": [top.R, top.Rq, top.n_runs],
+                                     "schedule_keys": ["R", "Rq", "n_runs"],
+                                     "predicted_ms": round(top.predicted_us / 1e3, 4),
+                                     "measured_ms": round(statistics.median(per_step_ms), 4)}
 
     gemm = decode = None
     if not args.no_secondary and rank == 0 and world == 1:
@@ -390,7 +535,6 @@ def run_gpu(args):
         cpu = {"value": round(rate, 6), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": sample, "seconds": round(dt, 2)}
 
-    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1) if rows else None
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -405,70 +549,13 @@ def run_gpu(args):
                            (q.numel() + k.numel() + v.numel()) * 2 >> 20)},
             "gpu_launches": args.steps * launches_per_step,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "secondary": secondary, "gemm": gemm, "decode": decode,
+            "configs": configs, "gemm": gemm, "decode": decode,
             "per_step_ms": {"min": round(min(per_step_ms), 4), "median": round(statistics.median(per_step_ms), 4),
                             "max": round(max(per_step_ms), 4)},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-def measure_merge_path(m, dev, stream, peaks, peak_kind, reps: int = 10):
-    """Partial + merge on the 2M-token MQA chunk: attention TFLOP/s of the
-    partial kernel and HBM GB/s of the merge (bytes: every partial read once,
-    the result written once)."""
-    import torch
-
-    from long_context_sharded_gb300.inputs import make_qkv
-    w = WORKLOADS[MERGE_WORKLOAD]
-    B, Hq, Hkv, Sq, Skv, d, R = w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], w["R"]
-    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=w["seed"], scale=w["scale"])
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    del q, k, v
-    op = torch.empty((R, B, Hq, Sq, d), dtype=torch.float32, device=dev)
-    lp = torch.empty((R, B, Hq, Sq), dtype=torch.float32, device=dev)
-    out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=dev)
-    for _ in range(3):
-        m.mercury_attn_partial(qd, kd, vd, R, w["shift"], w["causal"], op, lp, stream)
-        m.mercury_lse_merge(op, lp, out, lse, stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    t_part, t_merge = [], []
-    for _ in range(reps):
-        ev[0].record(stream)
-        m.mercury_attn_partial(qd, kd, vd, R, w["shift"], w["causal"], op, lp, stream)
-        ev[1].record(stream)
-        m.mercury_lse_merge(op, lp, out, lse, stream)
-        ev[2].record(stream)
-        torch.cuda.synchronize(dev)
-        t_part.append(ev[0].elapsed_time(ev[1]) / 1e3)
-        t_merge.append(ev[1].elapsed_time(ev[2]) / 1e3)
-    # the same chunk through mercury_attn_sharded: its schedule chooser cuts
-    # each rank's step sequence into runs and merges them (split-KV)
-    t_sh = []
-    for i in range(reps + 3):
-        ev[0].record(stream)
-        m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream)
-        ev[1].record(stream)
-        torch.cuda.synchronize(dev)
-        if i >= 3:
-            t_sh.append(ev[0].elapsed_time(ev[1]) / 1e3)
-    m.mercury_sync_status(stream)
-    rows = B * Hq * Sq
-    merge_bytes = R * rows * (4 * d + 4) + rows * (4 * d + 4)
-    tp, tm = statistics.median(t_part), statistics.median(t_merge)
-    flops = attention_flops(w)
-    gbs = merge_bytes / tm / 1e9
-    return {"workload": MERGE_WORKLOAD, "mode": "partial+merge",
-            "partial_ms": round(tp * 1e3, 4), "attention_tflops": round(flops / tp / 1e12, 2),
-            "attention_frac": round(flops / tp / 1e12 / peaks["bf16_tflops"], 4),
-            "merge_ms": round(tm * 1e3, 4), "merge_bytes": merge_bytes, "merge_gbs": round(gbs, 1),
-            "merge_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-            "total_tflops": round(flops / (tp + tm) / 1e12, 2),
-            "sharded_auto_ms": round(statistics.median(t_sh) * 1e3, 4),
-            "sharded_auto_tflops": round(flops / statistics.median(t_sh) / 1e12, 2),
-            "peak_kind": peak_kind, "reps": reps}
 
 
 def measure_gemm(m, dev, stream, peaks, peak_kind, reps: int = 10):
@@ -571,7 +658,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=BENCH_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true", help="do not run the host-buffer leg")
-    ap.add_argument("--no-secondary", action="store_true", help="do not run the partial+merge figure")
+    ap.add_argument("--no-configs", action="store_true", help="do not time the other workloads")
+    ap.add_argument("--no-secondary", action="store_true", help="do not time the GEMM and decode figures")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="do not time the CPU oracle")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
     args = ap.parse_args(argv)

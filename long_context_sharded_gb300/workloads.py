@@ -29,8 +29,9 @@ WORKLOADS = {
         scale=1.0, seed=5, mode="partial"),
 }
 
-# The workload the throughput benchmark times (Llama-3-8B-like GQA, 32K context).
-BENCH_WORKLOAD = "gqa_b1_hq32_hkv8_d128_s32k_causal_r8"
+# The workload the throughput benchmark times: the largest that fits one GPU
+# (Llama-3-70B-like GQA, 128K context, nested 2 x 4 shift).
+BENCH_WORKLOAD = "gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4"
 # The small workload every check can run in full on the CPU oracle.
 SMALL_WORKLOAD = "mha_b1_h4_d64_s512_r4"
 
