@@ -36,6 +36,10 @@
  *     error word and return early; that status is reported by
  *     mercury_sync_status().  With env MERCURY_SYNC_CHECK=1 every compute
  *     call synchronises its stream and returns the status itself.
+ *   - Test hook (env MERCURY_FAULT, unset in normal use): drop_p_arrive or
+ *     drop_kv_free makes the attention kernel withhold one internal arrive,
+ *     so the MMA issuer's or the TMA producer's bounded wait runs out and the
+ *     call ends with MERCURY_ETIMEOUT -- a timeout, never a GPU fault.
  */
 #ifndef MERCURY_ATTN_H
 #define MERCURY_ATTN_H
@@ -57,6 +61,8 @@ extern "C" {
 #define MERCURY_ETIMEOUT (-4)  /* a bounded device wait ran out                     */
 #define MERCURY_ENOMEM   (-5)  /* host-side allocation failed                       */
 #define MERCURY_EBUDGET  (-6)  /* no schedule fits the given device-memory budget   */
+#define MERCURY_EBOUNDS  (-7)  /* checked build only: an out-of-range index was
+                                  found in a kernel and its access skipped       */
 
 /* Largest number of virtual ranks a compute call accepts. */
 #define MERCURY_MAX_R 128
@@ -87,6 +93,14 @@ MERCURY_API int mercury_plan_shift(int R, int shift, int *order);
  * mercury_attn_sharded -- full attention through the shifted schedule, with
  * the per-step partials combined on the fly (online softmax across steps, the
  * same arithmetic as a log-sum-exp merge taken in step order).
+ *
+ * Passages: ranks consume the shared, sharded KV buffer in a rank-staggered
+ * order (Silicon & Systems, "The hidden cost of synchronized operators"),
+ * the shift primitive's (j+i)%J access gives the order (Mercury-SOSP25 paper
+ * notes, 核心方法), every step runs the same local attention patch
+ * (Silicon & Systems, "CommIR makes communication transformable"), and the
+ * result is checked against single-device FlashAttention, i.e. plain
+ * softmax attention (Silicon & Systems, "The tuning bill").
  *
  * Virtual rank i processes its query block against shards order[i][0..R-1]
  * (mercury_plan_shift(R, shift)); under causal masking a shard entirely in the
@@ -129,6 +143,12 @@ MERCURY_API int mercury_attn_sharded_bf16(const void *q, const void *k, const vo
 
 /*
  * mercury_attn_partial -- the per-step partials of the shifted schedule.
+ *
+ * Passages: each step's output is the local patch applied to one shard in
+ * the shifted order (Mercury-SOSP25 paper notes, 核心方法: shift, shard and
+ * the FlashAttention patch); combining the steps' partial results is what
+ * the RingAttention-style asynchronous schedules that Mercury reproduces do
+ * (Mercury-SOSP25 paper notes, one-line summary and 实验与结果).
  *
  * For every query row q (virtual rank i = q / (Sq/R)) and step j, slot j of
  * the outputs holds attention of that row over shard order[i][j] alone,
@@ -222,7 +242,14 @@ MERCURY_API int mercury_gemm_shifted(const void *a, const void *b, int M, int N,
  * runs * B*Hq*Sq*(d+1)*4 bytes; more than 64 MiB is rejected with
  * MERCURY_EINVAL before any work.
  * The first call on a device looks up the array's device address with that
- * device current; make it before any stream capture.  All calls on a device
+ * device current.  Under CUDA's lazy module loading (the default) that
+ * lookup also loads the array's module on the device, which reserves the
+ * 64 MiB: the first call can fail with MERCURY_ECUDA for lack of device
+ * memory.  A caller that must not allocate therefore makes one warm-up call
+ * on each device before it enters its allocation-free region (and before
+ * any stream capture); calls after that allocate nothing.  Waits and the
+ * test fault hook follow MERCURY_WAIT_NS and MERCURY_FAULT as for every
+ * other call.  All calls on a device
  * share the array: calls that can overlap on the GPU (other streams, other
  * threads) race and corrupt each other's results.  The array keeps the last
  * call's contents; nothing in it needs to start at zero, since each call
@@ -237,9 +264,12 @@ MERCURY_API int mercury_attn_split_noalloc(const void *q, const void *k, const v
 
 /*
  * mercury_sync_status -- synchronise `stream`, then read and clear the device
- * error word of this process's kernels.  Returns MERCURY_OK,
- * MERCURY_ETIMEOUT (a bounded device wait ran out in some earlier kernel) or
- * MERCURY_ECUDA (the synchronise itself failed).
+ * error words of this process's kernels.  Returns MERCURY_OK,
+ * MERCURY_ETIMEOUT (a bounded device wait ran out in some earlier kernel),
+ * MERCURY_EBOUNDS (only in the checked build, libmercury_attn.so built with
+ * -DMERCURY_CHECK: a kernel found an out-of-range TMA coordinate or output
+ * index and skipped that access) or MERCURY_ECUDA (the synchronise itself
+ * failed).
  */
 MERCURY_API int mercury_sync_status(void *stream);
 
@@ -400,10 +430,11 @@ MERCURY_API int mercury_attn_run_schedule(const void *q, const void *k, const vo
  * three timed launches each, CUDA events on `stream`, median -- and keeps the
  * fastest.  The choice is cached for the process under (device ordinal, SM
  * count, compute capability, library build, shape, R, shift, budget, top_k).
- * A later call with the same key runs the cached schedule once, timed; if it
- * takes more than 1.5 times its recorded time (env MERCURY_TUNE_RECHECK sets
- * the factor; 0 re-tunes on every call) the entry is dropped and the call
- * tunes again.  On return out / lse hold the attention result (from the
+ * A later call with the same key runs the cached schedule twice, timed; if
+ * the faster run takes more than 1.5 times its recorded time plus 20 us (an
+ * allowance for host launch jitter on very short calls; env
+ * MERCURY_TUNE_RECHECK sets the factor, 0 re-tunes on every call) the entry
+ * is dropped and the call tunes again.  On return out / lse hold the attention result (from the
  * chosen schedule's last run) and *best (if not NULL) the chosen schedule
  * with measured_us set.  *cache_hit (if not NULL) is 1 when no tuning ran.
  * The call synchronises `stream`.

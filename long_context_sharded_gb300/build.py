@@ -5,6 +5,12 @@ shared library with the CUDA runtime linked statically, so loading it needs no
 libcudart on the library path.  The tensor-map encoder is taken from the
 driver at run time (cudaGetDriverEntryPointByVersion), so there is no link-time
 dependency on libcuda either.
+
+build(check=True) makes the checked variant in _lib_check/: the same sources
+compiled with -DMERCURY_CHECK, whose kernels test every TMA coordinate and
+output index before using it and report a bad one as MERCURY_EBOUNDS instead
+of touching memory (a debugging build; the binding loads it when the
+environment sets MERCURY_CHECKED_BUILD=1).
 """
 from __future__ import annotations
 
@@ -17,6 +23,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmercury_attn.so")
+CHECK_LIB_DIR = os.path.join(HERE, "_lib_check")
+CHECK_LIB_PATH = os.path.join(CHECK_LIB_DIR, "libmercury_attn.so")
 SOURCES = ["api.cu", "attn_fwd.cu", "lse_merge.cu", "noalloc.cu", "gemm_shifted.cu", "schedule.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -36,23 +44,25 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, check: bool = False) -> str:
+    lib_dir, lib_path = (CHECK_LIB_DIR, CHECK_LIB_PATH) if check else (LIB_DIR, LIB_PATH)
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    obj_dir = os.path.join(LIB_DIR, "obj")
+    obj_dir = os.path.join(lib_dir, "obj")
     os.makedirs(obj_dir, exist_ok=True)
+    defines = ["-DMERCURY_CHECK"] if check else []
 
     def compile_one(src):
         obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed on %s:\n%s\n%s" % (src, r.stdout, r.stderr))
@@ -62,13 +72,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
+    tmp = lib_path + ".tmp%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

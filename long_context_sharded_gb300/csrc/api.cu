@@ -58,7 +58,9 @@ int fault_mode()
 {
     const char *e = getenv("MERCURY_FAULT");
     if (e && strcmp(e, "drop_p_arrive") == 0)
-        return 1;
+        return 1;  // a softmax warp withholds its first P-ready arrive: the MMA issuer's wait runs out
+    if (e && strcmp(e, "drop_kv_free") == 0)
+        return 2;  // the first "iteration done" arrive is withheld: the TMA producer's wait runs out
     return 0;
 }
 
@@ -122,17 +124,26 @@ int check_attn_args(const void *q, const void *k, const void *v, int B, int Hq, 
     return MERCURY_OK;
 }
 
-// Synchronise `stream` and collect the error words of every kernel module.
+// Synchronise `stream` and collect the error words of every kernel module
+// (bit 0: a bounded wait ran out; bit 1: the checked build skipped an
+// out-of-range access).
 int collect_device_errors(cudaStream_t stream)
 {
-    unsigned int w = 0, site = 0, w2 = 0, site2 = 0;
-    int rc = read_and_clear_device_error(stream, &w, &site, g_msg, sizeof g_msg);
+    unsigned int w[3] = {0, 0, 0}, site[3] = {0, 0, 0};
+    int rc = read_and_clear_device_error(stream, &w[0], &site[0], g_msg, sizeof g_msg);
     if (rc == MERCURY_OK)
-        rc = read_and_clear_gemm_error(&w2, &site2, g_msg, sizeof g_msg);
+        rc = read_and_clear_gemm_error(&w[1], &site[1], g_msg, sizeof g_msg);
+    if (rc == MERCURY_OK)
+        rc = read_and_clear_merge_error(&w[2], &site[2], g_msg, sizeof g_msg);
     if (rc != MERCURY_OK)
         return rc;
-    if ((w | w2) & 1u)
-        return fail(MERCURY_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", (w & 1u) ? site : site2);
+    for (int i = 0; i < 3; ++i)
+        if (w[i] & 2u)
+            return fail(MERCURY_EBOUNDS, "checked build: an out-of-range index was found and its access skipped "
+                        "(site 0x%x)", site[i]);
+    for (int i = 0; i < 3; ++i)
+        if (w[i] & 1u)
+            return fail(MERCURY_ETIMEOUT, "a bounded device wait ran out (site 0x%x)", site[i]);
     return MERCURY_OK;
 }
 
@@ -444,8 +455,8 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
                                float *lse, void *stream)
 {
     cudaStream_t s = (cudaStream_t)stream;
-    int rc = attn_split_noalloc(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_runs, out, lse, s,
-                                g_msg, sizeof g_msg);
+    int rc = attn_split_noalloc(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_runs, out, lse,
+                                wait_budget_ns(), fault_mode(), s, g_msg, sizeof g_msg);
     return finish(rc, s);
 }
 

@@ -32,7 +32,10 @@
 //
 // Every wait is bounded (%globaltimer); when one runs out the CTA records
 // MERCURY_ETIMEOUT in a device error word, raises a shared abort flag so the
-// other roles stop waiting too, frees its tensor memory and returns.
+// other roles stop waiting too, and leaves: the producer first waits (bounded
+// again) for the tile loads it has issued to land, the MMA issuer for the
+// tensor-core operations it has issued to complete, then every thread meets
+// at one exit barrier and the tensor memory is freed.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,19 +51,23 @@
 
 namespace mercury {
 
-// Device error word: bit 0 = a bounded wait ran out.  g_err_site keeps the
-// first site that timed out (for the error message).
+// Device error word: kErrTimeout = a bounded wait ran out; kErrBounds = the
+// checked build skipped an out-of-range access.  g_err_site keeps the first
+// site recorded (for the error message).
 __device__ unsigned int g_err_word = 0;
 __device__ unsigned int g_err_site = 0;
 
 struct AttnParams {
     Geom g;
     float scale_log2;        // log2(e) / sqrt(d)
-    int fault;               // test hook: 1 = drop the first P-ready arrive of tile 0
+    int fault;               // test hook: 1 = drop the first P-ready arrive of tile 0,
+                             // 2 = drop the first "iteration done" arrive (kv_free)
     int out_bf16;            // fused calls only: O is written as bf16 ([B,Hq,Sq,d], 2 bytes)
     int out_v8;              // O's base is 32-byte aligned: rows are stored 32 bytes per lane
     float *out;              // fused: out; partial: o_part
     float *lse;              // fused: lse; partial: lse_part
+    long long out_elems;     // elements of out / o_part (all slots); checked build only
+    long long lse_elems;     // elements of lse / lse_part (all slots); checked build only
     long long slot_o;        // partial: elements between slots of o_part
     long long slot_lse;      // partial: elements between slots of lse_part
     unsigned long long wait_ns;
@@ -82,6 +89,10 @@ struct Ctl {
     volatile uint32_t *abort;
 };
 
+// Exit barrier (named, all threads of the CTA; each role reaches it from its
+// own branch).
+constexpr uint32_t kExitBarrier = 1;
+
 // Bounded wait on an mbarrier phase.  false: timed out here or elsewhere.
 // Inlined: a call shared by warps with different setmaxnreg budgets does
 // not register-allocate.
@@ -99,11 +110,34 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Ctl c
             return false;
         if (globaltimer_ns() - t0 > c.budget) {
             *c.abort = 1u;
-            atomicOr(&g_err_word, 1u);
+            atomicOr(&g_err_word, kErrTimeout);
             atomicCAS(&g_err_site, 0u, site);
             return false;
         }
     }
+}
+
+// Checked build: an out-of-range index found at `site`.
+__device__ __forceinline__ void record_bounds(uint32_t site)
+{
+    atomicOr(&g_err_word, kErrBounds);
+    atomicCAS(&g_err_site, 0u, site);
+}
+
+// Bounded wait used on the way out: does not give up when another role
+// aborted (the operations it waits for complete on their own), only when its
+// own budget runs out, which it records like any other timeout.
+__device__ __forceinline__ bool drain_phase(uint64_t *bar, uint32_t parity, Ctl c, uint32_t site)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > c.budget) {
+            atomicOr(&g_err_word, kErrTimeout);
+            atomicCAS(&g_err_site, 0u, site);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Shard visited at step `step` of the item's sequence (fused: the rank's R
@@ -132,7 +166,7 @@ struct Smem {
     static constexpr int kOffV = kOffK + NK * kKVBytes;
     static constexpr int kOffBar = kOffV + NV * kKVBytes;
     static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
-    static constexpr int kNumBars = 1 + NK + NV + NE + 8;
+    static constexpr int kNumBars = 1 + NK + NV + NE + 8 + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem slot, abort flag
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -206,6 +240,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *p_full = s_full + 2;
     uint64_t *o_full = p_full + 2;
     uint64_t *o_free = o_full + 2;  // O_t read out by the softmax warps
+    uint64_t *mma_done = o_free + 2;  // every MMA the issuer issued has completed (exit)
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -228,6 +263,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             mbar_init(o_full + t, 1);
             mbar_init(o_free + t, 4);  // one arrive per softmax warp
         }
+        mbar_init(mma_done, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -251,6 +287,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             int g = 0;  // tile-iterations issued so far by this CTA
+            int nq = 0, nk = 0, nv = 0;  // Q, K and V loads issued (their barriers' phases)
             bool ok = true;
             for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
                 const Item it = decode_item(p.g, idx);
@@ -263,11 +300,27 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     ok = false;
                     break;
                 }
+                if (kChecked) {
+                    // each Q box: Gp heads x Mq rows x 64 columns; its heads must
+                    // be the item's batch's, its first row inside the sequence
+                    bool good = true;
+                    for (int t = 0; t < ntile; ++t)
+                        good = good && it.t[t].h0 + p.g.Gp <= p.g.Hq &&
+                               tma_coords_ok((NBOX - 1) * 64, it.t[t].q0, it.b * (long long)p.g.Hq + it.t[t].h0,
+                                             D, p.g.Sq, (long long)p.g.B * p.g.Hq, 0);
+                    if (!good) {
+                        record_bounds(0x501);
+                        *abort_flag = 1u;
+                        ok = false;
+                        break;
+                    }
+                }
                 mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQBytes));
                 for (int t = 0; t < ntile; ++t)
                     for (int c = 0; c < NBOX; ++c)
                         tma_load_3d(sQ + t * L::kQBytes + c * L::kBoxBytes, &tmQ, q_full, c * 64,
                                     it.t[t].q0, it.b * p.g.Hq + it.t[t].h0);
+                ++nq;
                 const int bkv = it.b * p.g.Hkv + it.hkv;
                 const int nsteps = item_steps(p.g, it);
                 for (int st = 0; st < nsteps && ok; ++st) {
@@ -275,6 +328,13 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     const int nt = step_range(p, it, st, lo, hi);
                     for (int tt = 0; tt < nt; ++tt, ++g) {
                         const int k0 = lo + tt * kTileKeys;
+                        if (kChecked && !tma_coords_ok((NBOX - 1) * 64, k0, bkv, D, p.g.Skv,
+                                                       (long long)p.g.B * p.g.Hkv, 0)) {
+                            record_bounds(0x502);
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
                         // stage g % NK held K(g - NK): free once iteration g - NK is done
                         const int ek = g - NK;
                         if (ek >= 0 && !wait_phase(kv_free + ek % NE, (ek / NE) & 1, ctl, 0x101)) {
@@ -286,6 +346,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         for (int c = 0; c < NBOX; ++c)
                             tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk, c * 64,
                                         k0, bkv);
+                        ++nk;
                         // stage g % NV held V(g - NV): free once iteration g - NV + 1 is done
                         const int ev = g - NV + 1;
                         if (g >= NV && !wait_phase(kv_free + ev % NE, (ev / NE) & 1, ctl, 0x102)) {
@@ -297,9 +358,26 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         for (int c = 0; c < NBOX; ++c)
                             tma_load_3d(sV + sv * L::kKVBytes + c * L::kBoxBytes, &tmV, v_full + sv, c * 64,
                                         k0, bkv);
+                        ++nv;
                     }
                 }
             }
+            // Before the CTA may leave, every load issued into its shared
+            // memory must have landed (after an abort some may still be in
+            // flight).  The last load of a stage is the newest phase of its
+            // barrier, so waiting for that phase covers the stage.
+            for (int s = 0; s < NK; ++s)
+                if (nk > s) {
+                    const int last = nk - 1 - ((nk - 1 - s) % NK);
+                    drain_phase(k_full + s, (last / NK) & 1, ctl, 0x111);
+                }
+            for (int s = 0; s < NV; ++s)
+                if (nv > s) {
+                    const int last = nv - 1 - ((nv - 1 - s) % NV);
+                    drain_phase(v_full + s, (last / NV) & 1, ctl, 0x112);
+                }
+            if (nq > 0)
+                drain_phase(q_full, (nq - 1) & 1, ctl, 0x113);
         } else if (warp == 1) {
             // --------------------------------------------------- MMA issuer
             // The whole warp runs this loop (its waits and descriptor
@@ -406,9 +484,21 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         ++g;
                 }
             }
+            // Every MMA this warp issued must complete before the tensor
+            // memory it writes is freed (after an abort some may be in flight).
+            umma_commit_w(mma_done, leader);
+            drain_phase(mma_done, 0, ctl, 0x211);
+            // and the arrives of its earlier commits must have landed
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (sp[t] > 0)
+                    drain_phase(s_full + t, (sp[t] - 1) & 1, ctl, 0x212);
+                if (od[t] > 0)
+                    drain_phase(o_full + t, (od[t] - 1) & 1, ctl, 0x213);
+            }
         }
         tc_fence_before();
-        __syncthreads();
+        named_barrier_sync(kExitBarrier, kThreads);
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, kTmemCols);
@@ -453,6 +543,15 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 }
                 orow = p.out + so + row * D;
                 lrow = p.lse + sl + row;
+                if (kChecked) {
+                    // element offsets (O may hold bf16 elements: same offsets)
+                    const long long oo = so + row * D, lo_ = sl + row;
+                    if (oo < 0 || oo + D > p.out_elems || lo_ < 0 || lo_ >= p.lse_elems) {
+                        record_bounds(0x503);
+                        orow = nullptr;
+                        lrow = nullptr;
+                    }
+                }
             }
             if (ntot == 0) {
                 // no allowed key for any row of this item in this shard
@@ -485,7 +584,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     }
                     ++sp;
                     tc_fence_after();
-                    if (forwards)
+                    if (forwards && !(p.fault == 2 && g + n == 0))
                         mbar_arrive(kv_free + (g + n) % NE);
                     uint32_t sr[128];
                     tmem_ld_x32x4(tS, sr);
@@ -664,7 +763,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
         tc_fence_before();
-        __syncthreads();
+        named_barrier_sync(kExitBarrier, kThreads);
     }
 }
 
@@ -763,6 +862,9 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     p.lse = c.lse;
     p.slot_o = (long long)c.B * c.Hq * c.Sq * c.d;
     p.slot_lse = (long long)c.B * c.Hq * c.Sq;
+    const int slots = c.mode == kFused ? 1 : p.g.n_groups;
+    p.out_elems = slots * p.slot_o;
+    p.lse_elems = slots * p.slot_lse;
     p.wait_ns = c.wait_ns;
     const int R = c.R;
     for (int i = 0; i < R; ++i)

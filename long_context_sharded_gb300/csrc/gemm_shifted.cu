@@ -34,8 +34,9 @@
 
 namespace mercury {
 
-// Device error word of this file's kernel (a module of its own): bit 0 = a
-// bounded wait ran out; the site of the first timeout.
+// Device error word of this file's kernel (a module of its own): kErrTimeout
+// = a bounded wait ran out, kErrBounds = the checked build skipped an
+// out-of-range access; the site of the first one recorded.
 __device__ unsigned int g_gemm_err_word = 0;
 __device__ unsigned int g_gemm_err_site = 0;
 
@@ -52,7 +53,8 @@ constexpr int kABytes = 2 * kAHalf;      // 32 KB
 constexpr int kBBytes = kBK * kBN * 2;   // 32 KB: four 64 x 64 boxes of 8 KB
 constexpr int kBBox = kBK * 64 * 2;      // 8 KB
 constexpr int kGOffBar = kStages * (kABytes + kBBytes);
-constexpr int kGBytes = kGOffBar + 8 * (2 * kStages + 4) + 16;
+constexpr int kGBytes = kGOffBar + 8 * (2 * kStages + 5) + 16;
+constexpr uint32_t kGExitBarrier = 1;  // named barrier of all threads at exit
 constexpr int kGAlloc = kGBytes + 1024;
 
 struct GemmParams {
@@ -82,11 +84,33 @@ __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, unsigned l
             return false;
         if (globaltimer_ns() - t0 > budget) {
             *abort = 1u;
-            atomicOr(&g_gemm_err_word, 1u);
+            atomicOr(&g_gemm_err_word, kErrTimeout);
             atomicCAS(&g_gemm_err_site, 0u, site);
             return false;
         }
     }
+}
+
+// Bounded wait on the way out: not cut short by another role's abort (the
+// operations it waits for complete on their own); a timeout is recorded.
+__device__ __forceinline__ bool gdrain(uint64_t *bar, uint32_t parity, unsigned long long budget, uint32_t site)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > budget) {
+            atomicOr(&g_gemm_err_word, kErrTimeout);
+            atomicCAS(&g_gemm_err_site, 0u, site);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Checked build: an out-of-range index found at `site`.
+__device__ __forceinline__ void grecord_bounds(uint32_t site)
+{
+    atomicOr(&g_gemm_err_word, kErrBounds);
+    atomicCAS(&g_gemm_err_site, 0u, site);
 }
 
 struct GTile {
@@ -124,7 +148,8 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 2;
-    uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
+    uint64_t *mma_done = acc_empty + 2;  // every MMA issued has completed (exit)
+    uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x / 32;
@@ -138,6 +163,7 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
             mbar_init(acc_full + a, 1);
             mbar_init(acc_empty + a, 4);  // one arrive per warp of that half's epilogue
         }
+        mbar_init(mma_done, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -165,6 +191,21 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     ok = false;
                     break;
                 }
+                if (kChecked) {
+                    // A boxes at (k, m) and (k, m + 128): the second half may hang
+                    // past M (zero fill); B boxes at (n + 64c, k)
+                    bool good = tma_coords_ok(kb * kBK, t.m0, 0, p.K, p.M, 1, 0) &&
+                                tma_coords_ok(kb * kBK, t.m0 + 128, 0, p.K, p.M, 1, kMmaM);
+                    for (int c = 0; c < kBN / 64; ++c)
+                        good = good && (t.n0 + c * 64 >= t.n_end ||
+                                        tma_coords_ok(t.n0 + c * 64, kb * kBK, 0, p.N, p.K, 1, 0));
+                    if (!good) {
+                        grecord_bounds(0x601);
+                        *abort_flag = 1u;
+                        ok = false;
+                        break;
+                    }
+                }
                 mbar_arrive_expect_tx(full + st, (uint32_t)(kABytes + kBBytes));
                 // A tile: [256 rows][64 k] as two boxes {64, 128} at (k, m), (k, m + 128)
                 tma_load_2d(sA + st * kABytes, &tmA, full + st, kb * kBK, t.m0);
@@ -174,6 +215,14 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     tma_load_2d(sB + st * kBBytes + c * kBBox, &tmB, full + st, t.n0 + c * 64, kb * kBK);
             }
         }
+        // every load issued into shared memory must land before the CTA
+        // leaves (after an abort some may be in flight): the last load of a
+        // stage is the newest phase of its barrier
+        for (int s = 0; s < kStages; ++s)
+            if (it > s) {
+                const int last = it - 1 - ((it - 1 - s) % kStages);
+                gdrain(full + s, (last / kStages) & 1, p.wait_ns, 0x411);
+            }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
         // (the whole warp runs the loop; one elected lane issues)
@@ -183,6 +232,8 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
         // boxes are kBBox bytes apart (leading-dimension offset)
         const uint64_t db = smem_desc_sw128(smem_u32(sB), kBBox, 1024);
         int it = 0, tile = 0;
+        int released = 0;          // stage releases committed (iterations 0 .. released-1)
+        int n_acc[2] = {0, 0};     // accumulator-ready commits per half
         bool ok = true;
         for (long long idx = blockIdx.x; idx < p.n_items && ok; idx += gridDim.x, ++tile) {
             for (int kb = 0; kb < p.KB && ok; ++kb, ++it) {
@@ -207,16 +258,27 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         umma_ss_w(tmem + h * kBN, das + (uint32_t)(kk * (32 >> 4)), dbs + (uint32_t)(kk * (2048 >> 4)),
                                 kIdesc, (kb > 0 || kk > 0) ? 1u : 0u, leader);
-                    if (kb == p.KB - 1)
+                    if (kb == p.KB - 1) {
                         umma_commit_w(acc_full + h, leader);  // this half is final: its epilogue may start
+                        ++n_acc[h];
+                    }
                 }
-                if (ok)
+                if (ok) {
                     umma_commit_w(empty + st, leader);
+                    ++released;
+                }
             }
         }
-        // let the last stage releases land before the CTA exits
-        for (int m = (it > kStages ? it - kStages : 0); m < it && ok; ++m)
-            ok = gwait(empty + (m % kStages), (m / kStages) & 1, p.wait_ns, abort_flag, 0x404);
+        // Before the CTA leaves (and the tensor memory is freed) every MMA
+        // issued must have completed and every commit's arrive have landed,
+        // also after an abort.
+        umma_commit_w(mma_done, leader);
+        gdrain(mma_done, 0, p.wait_ns, 0x404);
+        for (int m = (released > kStages ? released - kStages : 0); m < released; ++m)
+            gdrain(empty + (m % kStages), (m / kStages) & 1, p.wait_ns, 0x406);
+        for (int h = 0; h < 2; ++h)
+            if (n_acc[h] > 0)
+                gdrain(acc_full + h, (n_acc[h] - 1) & 1, p.wait_ns, 0x407);
     } else if (warp >= 4) {
         // ----------------------------------------------------- epilogue
         const int acc = (warp - 4) / 4;  // the 128-row half this warpgroup writes
@@ -234,9 +296,18 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
             }
             tc_fence_after();
             const int row = t.m0 + r;
-            const bool row_ok = row < t.m_end && row < p.M;
+            bool row_ok = row < t.m_end && row < p.M;
             const int n_lim = min(t.n_end, p.N) - t.n0;  // valid columns of this tile
             float *crow = p.c + (long long)row * p.N + t.n0;
+            if (kChecked && row_ok) {
+                // the row's stores cover columns [n0, n0 + min(n_lim, 256))
+                const long long first = (long long)row * p.N + t.n0;
+                const long long last = first + min(n_lim, kBN);
+                if (row < 0 || t.n0 < 0 || n_lim < 0 || last > (long long)p.M * p.N) {
+                    grecord_bounds(0x602);
+                    row_ok = false;
+                }
+            }
 #pragma unroll 1
             for (int c0 = 0; c0 < kBN; c0 += 32) {
                 uint32_t v[32];
@@ -268,7 +339,7 @@ gemm_shifted_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
         }
     }
     tc_fence_before();
-    __syncthreads();
+    named_barrier_sync(kGExitBarrier, kGThreads);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);

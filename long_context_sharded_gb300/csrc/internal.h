@@ -28,10 +28,11 @@ int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, lo
                      float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len, int out_bf16 = 0);
 
 // The split-KV schedule with its partials in the library's fixed-size
-// device array instead of allocated scratch (noalloc.cu).
+// device array instead of allocated scratch (noalloc.cu).  wait_ns and fault
+// as in AttnCall.
 int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                        int d, int R, int shift, int causal, int n_runs, float *out, float *lse,
-                       cudaStream_t stream, char *msg, size_t msg_len);
+                       unsigned long long wait_ns, int fault, cudaStream_t stream, char *msg, size_t msg_len);
 
 // Shifted-shard GEMM: C [M,N] fp32 = A [M,K] bf16 x B [K,N] bf16; rank i's
 // row block against B's column shards in the order order[i][*].
@@ -40,6 +41,9 @@ int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R
 
 // Read and clear the GEMM kernel's device error word (no synchronisation).
 int read_and_clear_gemm_error(unsigned int *word, unsigned int *site, char *msg, size_t msg_len);
+
+// Read and clear the merge kernel's device error word (no synchronisation).
+int read_and_clear_merge_error(unsigned int *word, unsigned int *site, char *msg, size_t msg_len);
 
 // Synchronise `stream`, read and clear the kernels' device error word.
 int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,

@@ -19,9 +19,22 @@
 #include <stdio.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mercury {
+
+// Device error word of this file's kernel (a module of its own): kErrBounds
+// = the checked build skipped an out-of-range access; the first site.
+__device__ unsigned int g_merge_err_word = 0;
+__device__ unsigned int g_merge_err_site = 0;
+
 namespace {
+
+__device__ __forceinline__ void mrecord_bounds(uint32_t site)
+{
+    atomicOr(&g_merge_err_word, kErrBounds);
+    atomicCAS(&g_merge_err_site, 0u, site);
+}
 
 constexpr int kMergeThreads = 256;
 
@@ -65,6 +78,17 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
         acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     const long long part_stride = rows * (long long)d;
     const float4 *src = reinterpret_cast<const float4 *>(o_part + row * (long long)d);
+    // checked build: every part's row read and the output row written lie
+    // inside their arrays (element offsets of the row's first and last float4)
+    bool row_ok = active;
+    if (kChecked && active) {
+        const long long first = row * (long long)d, last_read = (long long)(n_parts - 1) * part_stride + first + d;
+        if (row < 0 || first + d > rows * (long long)d || last_read > (long long)n_parts * part_stride ||
+            (d % 4) != 0) {
+            mrecord_bounds(0x701);
+            row_ok = false;
+        }
+    }
     for (int j0 = 0; j0 < n_parts; j0 += TPR) {
         // lane g of the group holds the weight of part j0 + g
         float w_mine = 0.f;
@@ -74,7 +98,7 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
 #pragma unroll 4
         for (int jj = 0; jj < cnt; ++jj) {
             const float w = __shfl_sync(full, w_mine, grp_base + jj);
-            if (active && w != 0.f) {
+            if (row_ok && w != 0.f) {
                 const float4 *s = src + (long long)(j0 + jj) * (part_stride / 4);
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) {
@@ -90,7 +114,7 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
             }
         }
     }
-    if (active && out_bf16) {
+    if (row_ok && out_bf16) {
         // out holds bf16: four elements (8 bytes) per float4 of the row
         uint2 *dst = reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + row * (long long)d);
 #pragma unroll
@@ -102,7 +126,7 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
                 dst[c] = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
             }
         }
-    } else if (active) {
+    } else if (row_ok) {
         float4 *dst = reinterpret_cast<float4 *>(out + row * (long long)d);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
@@ -111,7 +135,7 @@ lse_merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse
                 dst[c] = acc[v];
         }
     }
-    if (active) {
+    if (row_ok) {
         if (g == 0)
             lse[row] = L;
     }
@@ -138,6 +162,26 @@ int launch(const float *o_part, const float *lse_part, int n_parts, long long ro
 }
 
 }  // namespace
+
+int read_and_clear_merge_error(unsigned int *word, unsigned int *site, char *msg, size_t msg_len)
+{
+    unsigned int zero = 0, w = 0, st = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&w, g_merge_err_word, sizeof w);
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(&st, g_merge_err_site, sizeof st);
+    if (e == cudaSuccess && (w || st)) {
+        e = cudaMemcpyToSymbol(g_merge_err_word, &zero, sizeof zero);
+        if (e == cudaSuccess)
+            e = cudaMemcpyToSymbol(g_merge_err_site, &zero, sizeof zero);
+    }
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "reading the merge error word: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    *word = w;
+    *site = st;
+    return MERCURY_OK;
+}
 
 int launch_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
                      float *out, float *lse, cudaStream_t stream, char *msg, size_t msg_len, int out_bf16)

@@ -15,8 +15,12 @@
 //  * the scratch is kNoAllocScratchBytes (64 MiB) per device; a call whose
 //    partials do not fit is rejected with MERCURY_EINVAL before any work;
 //  * the first call on a device looks up the array's device address
-//    (cudaGetSymbolAddress) with that device current; make that first call
-//    before any stream capture;
+//    (cudaGetSymbolAddress) with that device current.  With CUDA's lazy
+//    module loading (the default) that lookup is also what loads this file's
+//    module on the device and so reserves the 64 MiB: the first call can fail
+//    for lack of device memory, and a caller that must not allocate makes one
+//    warm-up call before it enters its allocation-free region (and before any
+//    stream capture).  Calls after that allocate nothing;
 //  * every call on a device uses the same array: calls that may overlap on
 //    the GPU (different streams, or threads without ordering) race and give
 //    wrong results; the array keeps the last call's contents, and nothing in
@@ -82,7 +86,7 @@ bool aligned(const void *p, uintptr_t a)
 
 int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                        int d, int R, int shift, int causal, int n_runs, float *out, float *lse,
-                       cudaStream_t stream, char *msg, size_t msg_len)
+                       unsigned long long wait_ns, int fault, cudaStream_t stream, char *msg, size_t msg_len)
 {
     if (!q || !k || !v || !out || !lse) {
         snprintf(msg, msg_len, "null pointer argument");
@@ -154,8 +158,8 @@ int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int H
     c.order = order;
     c.out = o_part;
     c.lse = l_part;
-    c.wait_ns = 2000000000ull;
-    c.fault = 0;
+    c.wait_ns = wait_ns;
+    c.fault = fault;
     rc = launch_attention(c, stream, msg, msg_len);
     if (rc == MERCURY_OK)
         rc = launch_lse_merge(o_part, l_part, g.n_groups, rows, d, out, lse, stream, msg, msg_len);

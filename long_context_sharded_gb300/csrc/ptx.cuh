@@ -7,6 +7,29 @@
 
 namespace mercury {
 
+// Checked build (compiled with -DMERCURY_CHECK): the kernels test every TMA
+// tile coordinate and every output store index before using it.  A bad one
+// sets kErrBounds in the kernel's device error word (with the site of the
+// check) and the access is skipped -- no trap, no fault; the host reports
+// MERCURY_EBOUNDS.  In the normal build the checks compile away.
+#ifdef MERCURY_CHECK
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr unsigned int kErrTimeout = 1u;  // a bounded wait ran out
+constexpr unsigned int kErrBounds = 2u;   // a checked index was out of range (access skipped)
+
+// A tiled TMA load at (x, y, z) of a [dz][dy][dx] bf16 tensor: x (innermost,
+// in elements) must be 16-byte aligned and inside the tensor, z inside, and y
+// inside or at most y_over rows past the end (a tile hanging off the end of
+// the tensor is zero-filled there, which the kernels use for ragged tails).
+__device__ __forceinline__ bool tma_coords_ok(long long x, long long y, long long z, long long dx, long long dy,
+                                              long long dz, long long y_over)
+{
+    return x >= 0 && x < dx && (x % 8) == 0 && y >= 0 && y < dy + y_over && z >= 0 && z < dz;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -53,6 +76,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// Named barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads, a
+// multiple of 32.  Each thread arrives on its own, so warps whose lanes
+// reach it at different times (one lane ran a producer loop) are fine.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA

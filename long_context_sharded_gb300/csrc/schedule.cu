@@ -349,9 +349,13 @@ std::map<std::string, mercury_schedule> g_cache;
 
 const char *kBuildId = __DATE__ " " __TIME__;
 
-// A cached schedule is kept while a re-timed run takes at most this factor
-// of its recorded time (1.5; env MERCURY_TUNE_RECHECK overrides, 0 forces a
-// re-tune on every call).
+// A cached schedule is kept while the faster of two re-timed runs takes at
+// most this factor of its recorded time (1.5; env MERCURY_TUNE_RECHECK
+// overrides, 0 forces a re-tune on every call), plus kRecheckSlackUs: a
+// single run of a call of a few tens of microseconds can take that much more
+// when the host is late to launch it, which says nothing about the schedule.
+constexpr double kRecheckSlackUs = 20.0;
+
 double recheck_factor()
 {
     const char *e = getenv("MERCURY_TUNE_RECHECK");
@@ -597,10 +601,13 @@ int mercury_tune_schedule(const void *q, const void *k, const void *v, int B, in
         }
     }
     if (have) {
-        double t = 0;
-        if ((rc = time_median(runner(cached), 0, 1, s, ev, &t)))
+        double t = 0, t2 = 0;
+        if ((rc = time_median(runner(cached), 0, 1, s, ev, &t)) ||
+            (rc = time_median(runner(cached), 0, 1, s, ev, &t2)))
             return rc;
-        if (t <= recheck_factor() * cached.measured_us) {
+        t = std::min(t, t2);
+        const double factor = recheck_factor();
+        if (factor > 0 && t <= factor * cached.measured_us + kRecheckSlackUs) {
             if ((rc = check_errors_after(s)))
                 return rc;
             if (best)

@@ -32,11 +32,13 @@ MERCURY_ECUDA = -3
 MERCURY_ETIMEOUT = -4
 MERCURY_ENOMEM = -5
 MERCURY_EBUDGET = -6
+MERCURY_EBOUNDS = -7
 MERCURY_MAX_R = 128
 
 _STATUS_NAMES = {
     MERCURY_EINVAL: "EINVAL", MERCURY_EALIGN: "EALIGN", MERCURY_ECUDA: "ECUDA",
     MERCURY_ETIMEOUT: "ETIMEOUT", MERCURY_ENOMEM: "ENOMEM", MERCURY_EBUDGET: "EBUDGET",
+    MERCURY_EBOUNDS: "EBOUNDS",
 }
 
 # Every symbol include/mercury_attn.h declares.
@@ -78,12 +80,16 @@ class MercuryError(RuntimeError):
         self.status = status
 
 
+# MERCURY_CHECKED_BUILD=1 loads the bounds-checked variant (build(check=True)).
+CHECKED = os.environ.get("MERCURY_CHECKED_BUILD", "") == "1"
+
+
 def _load() -> ctypes.CDLL:
-    path = _build.LIB_PATH
+    path = _build.CHECK_LIB_PATH if CHECKED else _build.LIB_PATH
     if not os.path.exists(path):
         raise ImportError(
-            "libmercury_attn.so is not built (%s); run long_context_sharded_gb300.build.build() "
-            "or __graft_entry__.build() first" % path)
+            "libmercury_attn.so is not built (%s); run long_context_sharded_gb300.build.build(%s) "
+            "or __graft_entry__.build() first" % (path, "check=True" if CHECKED else ""))
     lib = ctypes.CDLL(path)
     i32, i64, p = ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p
     attn_args = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32, p, p, p]
@@ -135,6 +141,9 @@ def _stream_ptr(stream):
 
 
 def _dev_ptr(t, dtype_name, what):
+    """Device pointer of a contiguous CUDA tensor of the given dtype on the
+    current device (the library runs on the current device, and a pointer
+    into another device's memory would be read there)."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch tensor" % what)
@@ -144,7 +153,22 @@ def _dev_ptr(t, dtype_name, what):
         raise TypeError("%s must be %s (got %s)" % (what, dtype_name, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % what)
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError("%s is on %s but the current device is cuda:%d" % (what, t.device, cur))
     return t.data_ptr()
+
+
+def _check_shape(t, shape, what):
+    """A caller-provided output must have exactly the shape the call writes:
+    the kernels write every element of that shape, so a smaller buffer would
+    be overrun."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % what)
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError("%s must have shape %s (got %s)" % (what, tuple(int(x) for x in shape),
+                                                            tuple(t.shape)))
 
 
 def mercury_plan_shift(R: int, shift: int) -> np.ndarray:
@@ -173,6 +197,8 @@ def mercury_attn_sharded(q, k, v, R: int, shift: int, causal: bool, out=None, ls
         out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     rc = lib.mercury_attn_sharded(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
@@ -191,6 +217,8 @@ def mercury_attn_sharded_bf16(q, k, v, R: int, shift: int, causal: bool, out=Non
         out = torch.empty((B, Hq, Sq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     rc = lib.mercury_attn_sharded_bf16(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
@@ -209,6 +237,8 @@ def mercury_attn_partial(q, k, v, R: int, shift: int, causal: bool, o_part=None,
         o_part = torch.empty((R, B, Hq, Sq, d), dtype=torch.float32, device=q.device)
     if lse_part is None:
         lse_part = torch.empty((R, B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(o_part, (R, B, Hq, Sq, d), "o_part")
+    _check_shape(lse_part, (R, B, Hq, Sq), "lse_part")
     rc = lib.mercury_attn_partial(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
@@ -230,6 +260,10 @@ def mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None):
         out = torch.empty(tuple(o_part.shape[1:]), dtype=torch.float32, device=o_part.device)
     if lse is None:
         lse = torch.empty(tuple(lse_part.shape[1:]), dtype=torch.float32, device=o_part.device)
+    if out.numel() != rows * d or out.shape[-1] != d:
+        raise ValueError("out must hold %d rows of %d (got shape %s)" % (rows, d, tuple(out.shape)))
+    if lse.numel() != rows:
+        raise ValueError("lse must hold %d rows (got shape %s)" % (rows, tuple(lse.shape)))
     rc = lib.mercury_lse_merge(
         _dev_ptr(o_part, "torch.float32", "o_part"), _dev_ptr(lse_part, "torch.float32", "lse_part"),
         n_parts, rows, d, _dev_ptr(out, "torch.float32", "out"),
@@ -244,6 +278,8 @@ def mercury_attn_split_noalloc(q, k, v, R: int, shift: int, causal: bool, n_runs
     device array: no device memory is allocated (out and lse are the
     caller's).  Calls that may overlap on the GPU must not share a device."""
     B, Hq, Hkv, Sq, Skv, d = _shapes(q, k, v)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     rc = lib.mercury_attn_split_noalloc(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, R, shift, int(bool(causal)),
@@ -261,6 +297,8 @@ def mercury_attn_decode(q, k, v, n_splits: int = 0, causal: bool = False, out=No
         out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     rc = lib.mercury_attn_decode(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
         _dev_ptr(v, "torch.bfloat16", "v"), B, Hq, Hkv, Sq, Skv, d, int(n_splits), int(bool(causal)),
@@ -278,6 +316,7 @@ def mercury_gemm_shifted(a, b, R: int, shift: int, c=None, stream=None):
     N = b.shape[1]
     if c is None:
         c = torch.empty((M, N), dtype=torch.float32, device=a.device)
+    _check_shape(c, (M, N), "c")
     rc = lib.mercury_gemm_shifted(_dev_ptr(a, "torch.bfloat16", "a"), _dev_ptr(b, "torch.bfloat16", "b"),
                                   M, N, K, R, shift, _dev_ptr(c, "torch.float32", "c"), _stream_ptr(stream))
     _check(rc)
@@ -348,6 +387,8 @@ def mercury_attn_run_schedule(q, k, v, causal: bool, plan, out=None, lse=None, s
         out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     plan = _schedule(plan)
     rc = lib.mercury_attn_run_schedule(
         _dev_ptr(q, "torch.bfloat16", "q"), _dev_ptr(k, "torch.bfloat16", "k"),
@@ -367,6 +408,8 @@ def mercury_tune_schedule(q, k, v, R: int, shift: int, causal: bool, budget_byte
         out = torch.empty((B, Hq, Sq, d), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check_shape(out, (B, Hq, Sq, d), "out")
+    _check_shape(lse, (B, Hq, Sq), "lse")
     best = Schedule()
     hit = ctypes.c_int(0)
     rc = lib.mercury_tune_schedule(

@@ -107,6 +107,34 @@ def test_merge_argument_validation(m, args, code):
     assert m.lib.mercury_lse_merge(*args, None) == code
 
 
+def call_noalloc(m, q=P, k=P, v=P, out=P, lse=P, n_runs=2, **kw):
+    a = dict(GOOD, **kw)
+    return m.lib.mercury_attn_split_noalloc(q, k, v, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["d"],
+                                            a["R"], a["shift"], a["causal"], n_runs, out, lse, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), -1), (dict(k=0), -1), (dict(v=0), -1), (dict(out=0), -1), (dict(lse=0), -1),
+    (dict(d=96), -1), (dict(n_runs=0), -1), (dict(n_runs=5), -1), (dict(R=0), -1), (dict(R=129), -1),
+    (dict(shift=3), -1), (dict(causal=1, Sq=512, Skv=256), -1), (dict(Sq=250), -1), (dict(Hq=6, Hkv=4), -1),
+    (dict(q=P + 2), -2), (dict(k=P + 8), -2), (dict(v=P + 4), -2), (dict(out=P + 4), -2), (dict(lse=P + 2), -2),
+])
+def test_noalloc_argument_validation(m, kw, code):
+    """The allocation-free entry point rejects bad arguments before any CUDA
+    call (so these run without a GPU)."""
+    assert call_noalloc(m, **kw) == code
+    assert m.lib.mercury_last_error()
+
+
+@pytest.mark.parametrize("n_runs", [64, 8])
+def test_noalloc_rejects_partials_beyond_its_array(m, n_runs):
+    # n_runs x 8*2048 rows x (128+1) x 4 bytes: 541 MB and 68 MB, both over 64 MiB
+    rc = call_noalloc(m, B=1, Hq=8, Hkv=1, Sq=2048, Skv=8192, d=128, R=64, n_runs=n_runs)
+    assert rc == m.MERCURY_EINVAL
+    msg = m.lib.mercury_last_error()
+    assert b"scratch" in msg and b"67108864" in msg
+
+
 def test_merge_zero_rows_is_noop(m):
     assert m.lib.mercury_lse_merge(P, P, 4, 0, 128, P, P, None) == 0
 

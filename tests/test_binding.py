@@ -25,7 +25,56 @@ def _qkv(dtype=torch.bfloat16, device="cpu"):
 def test_cpu_tensors_rejected(m):
     q, k, v = _qkv()
     with pytest.raises(ValueError, match="CUDA"):
-        m.mercury_attn_sharded(q, k, v, 4, 1, False, out=torch.zeros(1), lse=torch.zeros(1))
+        m.mercury_attn_sharded(q, k, v, 4, 1, False, out=torch.zeros(1, 4, 256, 128),
+                               lse=torch.zeros(1, 4, 256))
+
+
+def _outs(shape_o=(1, 4, 256, 128), shape_l=(1, 4, 256), dtype=torch.float32):
+    return torch.zeros(shape_o, dtype=dtype), torch.zeros(shape_l)
+
+
+@pytest.mark.parametrize("call", ["sharded", "sharded_bf16", "split_noalloc", "decode", "run_schedule",
+                                  "tune_schedule"])
+@pytest.mark.parametrize("which", ["out", "lse"])
+def test_undersized_outputs_rejected_before_the_library(m, monkeypatch, call, which):
+    """A caller-provided out or lse smaller (or larger) than [B,Hq,Sq,d] /
+    [B,Hq,Sq] would be written past its end: the binding refuses it before
+    any pointer reaches the library."""
+    def no_call(*a, **kw):
+        raise AssertionError("the library was called")
+    monkeypatch.setattr(m, "lib", type("NoLib", (), {n: staticmethod(no_call) for n in m.EXPORTED})())
+    q, k, v = _qkv()
+    dt = torch.bfloat16 if call == "sharded_bf16" else torch.float32
+    out, lse = _outs(dtype=dt)
+    if which == "out":
+        out = torch.zeros((1, 4, 255, 128), dtype=dt)
+    else:
+        lse = torch.zeros((1, 4, 128))
+    fn = {"sharded": lambda: m.mercury_attn_sharded(q, k, v, 4, 1, False, out, lse),
+          "sharded_bf16": lambda: m.mercury_attn_sharded_bf16(q, k, v, 4, 1, False, out, lse),
+          "split_noalloc": lambda: m.mercury_attn_split_noalloc(q, k, v, 4, 1, False, 2, out, lse),
+          "decode": lambda: m.mercury_attn_decode(q, k, v, 0, False, out, lse),
+          "run_schedule": lambda: m.mercury_attn_run_schedule(q, k, v, False, (4, 4, 1, 1), out, lse),
+          "tune_schedule": lambda: m.mercury_tune_schedule(q, k, v, 4, 1, False, 0, 2, out, lse)}[call]
+    with pytest.raises(ValueError, match="%s must have shape" % which):
+        fn()
+
+
+def test_partial_and_merge_output_shapes_checked(m):
+    q, k, v = _qkv()
+    with pytest.raises(ValueError, match="o_part must have shape"):
+        m.mercury_attn_partial(q, k, v, 4, 1, False, torch.zeros(3, 1, 4, 256, 128), torch.zeros(4, 1, 4, 256))
+    with pytest.raises(ValueError, match="lse_part must have shape"):
+        m.mercury_attn_partial(q, k, v, 4, 1, False, torch.zeros(4, 1, 4, 256, 128), torch.zeros(4, 1, 4, 255))
+    o = torch.zeros(4, 10, 128)
+    lp = torch.zeros(4, 10)
+    with pytest.raises(ValueError, match="out must hold"):
+        m.mercury_lse_merge(o, lp, torch.zeros(9, 128), torch.zeros(10))
+    with pytest.raises(ValueError, match="lse must hold"):
+        m.mercury_lse_merge(o, lp, torch.zeros(10, 128), torch.zeros(9))
+    with pytest.raises(ValueError, match="c must have shape"):
+        m.mercury_gemm_shifted(torch.zeros(16, 8, dtype=torch.bfloat16), torch.zeros(8, 32, dtype=torch.bfloat16),
+                               2, 1, torch.zeros(16, 31))
 
 
 def test_shape_mismatch_rejected(m):

@@ -304,6 +304,55 @@ def test_output_canaries_untouched(m):
     assert (big_o[n_o:] == 7.25).all() and (big_l[n_l:] == 7.25).all()
 
 
+def _guarded(n, dtype, fill=7.25, pad=4096):
+    """A buffer of n elements with `pad` canary elements on each side."""
+    big = torch.full((n + 2 * pad,), fill, dtype=dtype, device="cuda")
+    return big, big[pad:pad + n]
+
+
+def _canaries_intact(big, n, fill=7.25, pad=4096):
+    return bool((big[:pad] == fill).all()) and bool((big[pad + n:] == fill).all())
+
+
+@pytest.mark.parametrize("cfg", [(1, 4, 2, 320, 320, 128, 2, 1, True), (1, 8, 1, 96, 3072, 64, 3, 1, False)],
+                         ids=["gqa_causal", "mqa_packed"])
+def test_partial_and_merge_canaries_untouched(m, cfg):
+    """Per-step partials (every slot) and the merge's outputs are written
+    inside their arrays only: canaries on both sides stay intact."""
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=17)
+    rows = B * Hq * Sq
+    bo, op = _guarded(R * rows * d, torch.float32)
+    bl, lp = _guarded(R * rows, torch.float32)
+    m.mercury_attn_partial(q.cuda(), k.cuda(), v.cuda(), R, shift, causal, op.view(R, B, Hq, Sq, d),
+                           lp.view(R, B, Hq, Sq))
+    bmo, mo = _guarded(rows * d, torch.float32)
+    bml, ml = _guarded(rows, torch.float32)
+    m.mercury_lse_merge(op.view(R, B, Hq, Sq, d), lp.view(R, B, Hq, Sq), mo.view(B, Hq, Sq, d), ml.view(B, Hq, Sq))
+    m.mercury_sync_status()
+    assert _canaries_intact(bo, R * rows * d) and _canaries_intact(bl, R * rows)
+    assert _canaries_intact(bmo, rows * d) and _canaries_intact(bml, rows)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    assert_close(mo.cpu().numpy(), ml.cpu().numpy(), o_ref, l_ref, "merge inside canaries")
+
+
+@pytest.mark.parametrize("groups", [1, 3], ids=["fused", "split3"])
+def test_bf16_output_canaries_untouched(m, groups, monkeypatch):
+    """bf16 O (fused, or split runs merged then rounded) stays inside its array."""
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", str(groups))
+    B, Hq, Hkv, S, d, R = 1, 4, 2, 384, 128, 3
+    q, k, v = make_qkv(B, Hq, Hkv, S, S, d, seed=19)
+    n_o, n_l = B * Hq * S * d, B * Hq * S
+    bo, out = _guarded(n_o, torch.bfloat16)
+    bl, lse = _guarded(n_l, torch.float32)
+    m.mercury_attn_sharded_bf16(q.cuda(), k.cuda(), v.cuda(), R, 1, True, out.view(B, Hq, S, d),
+                                lse.view(B, Hq, S))
+    m.mercury_sync_status()
+    assert _canaries_intact(bo, n_o) and _canaries_intact(bl, n_l)
+    o_ref, l_ref = oracle.attn(q, k, v, True)
+    assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "bf16 inside canaries")
+
+
 @pytest.mark.parametrize("bf16", [False, True], ids=["fp32_out", "bf16_out"])
 def test_output_16_byte_aligned_only(m, bf16, monkeypatch):
     """O at an address that is 16- but not 32-byte aligned takes the 16-byte
@@ -353,17 +402,22 @@ def test_lse_merge_matches_oracle(m, n_parts, rows, d):
 
 # ------------------------------------------------------ fault path (no GPU fault)
 
-def test_bounded_wait_times_out_cleanly(m, monkeypatch):
+@pytest.mark.parametrize("fault", ["drop_p_arrive", "drop_kv_free"])
+def test_bounded_wait_times_out_cleanly(m, monkeypatch, fault):
     """A dropped arrive makes a device wait run out: the kernel records
-    ETIMEOUT and returns; the context stays usable for the next call."""
+    ETIMEOUT and returns; the context stays usable for the next call.
+    drop_p_arrive starves the MMA issuer; drop_kv_free starves the TMA
+    producer after it has issued loads, so its exit path (wait for the loads
+    it issued to land) runs too."""
     q, k, v = make_qkv(1, 2, 1, 512, 512, 128, seed=1)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    monkeypatch.setenv("MERCURY_FAULT", "drop_p_arrive")
+    monkeypatch.setenv("MERCURY_FAULT", fault)
     monkeypatch.setenv("MERCURY_WAIT_NS", "20000000")
     m.mercury_attn_sharded(qd, kd, vd, 2, 1, False)
     with pytest.raises(m.MercuryError) as e:
         m.mercury_sync_status()
     assert e.value.status == m.MERCURY_ETIMEOUT
+    assert "site 0x" in str(e.value)
     monkeypatch.delenv("MERCURY_FAULT")
     monkeypatch.delenv("MERCURY_WAIT_NS")
     out, lse = m.mercury_attn_sharded(qd, kd, vd, 2, 1, False)
