@@ -20,9 +20,14 @@ reported.
 
 Metric: attention TFLOP/s = 4 * d * (unmasked query/key pairs) * B * Hq per
 step / time.  Inputs (2.5 GiB on the headline) are larger than L2, so no flush
-is needed between steps.  Several GPUs (torchrun) run independent replicas:
-the path needs no exchange on one GPU per replica, so value = sum of all
-ranks' work / max-over-ranks time ("weak" scaling).
+is needed between steps.
+
+Several GPUs (torchrun): by default virtual rank i lives on GPU i -- query
+block i and KV shard i stay there and the KV shards travel between GPUs in the
+shifted order (NCCL point to point, transport.py), the workload split over
+the GPUs ("strong" scaling, value = the workload's FLOPs / the slowest rank's
+time).  --dist-mode replicas runs independent copies of the one-GPU step
+instead ("weak" scaling: all ranks' work / the slowest rank's time).
 """
 from __future__ import annotations
 
@@ -558,6 +563,114 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------- N GPUs: the shifted exchange
+
+def dist_shift_for(world: int, shift: int) -> int:
+    """Shift order across `world` devices: the workload's nested inner size
+    when it divides the device count into two or more groups, else flat."""
+    if shift >= 2 and world % shift == 0 and world > shift:
+        return shift
+    return 1
+
+
+def local_block(t, rank: int, world: int):
+    """Rank `rank`'s contiguous block of the sequence axis (dim 2) of t."""
+    n = t.shape[2] // world
+    return t[:, :, rank * n:(rank + 1) * n].contiguous()
+
+
+def run_gpu_shifted(args):
+    """Virtual rank i on GPU i: query block i and KV shard i stay on GPU i,
+    the shards travel between GPUs in the shifted order (NCCL point to point
+    into a local double buffer, see transport.py) and every GPU runs the
+    local patch and the merge on its own memory.  The whole workload is split
+    over the GPUs, so the scaling is strong; value = the workload's FLOPs per
+    step / the slowest rank's time."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    dist = init_dist(world, "nccl")
+    from long_context_sharded_gb300 import mercury as m  # noqa: F401  (loads the library)
+    from long_context_sharded_gb300 import transport as tp
+    from long_context_sharded_gb300.inputs import make_qkv
+
+    w = dict(WORKLOADS[args.workload], name=args.workload)
+    B, Hq, Hkv, Sq, Skv, d, causal = w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], w["causal"]
+    if Sq % world or Skv % world or (causal and Sq != Skv):
+        raise SystemExit("workload %s cannot be split over %d GPUs" % (args.workload, world))
+    shift = dist_shift_for(world, w["shift"])
+    flops = attention_flops(w)
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=w["seed"], scale=w["scale"])
+    qh, kh, vh = (local_block(t, rank, world) for t in (q, k, v))
+    del q, k, v
+    qb, kb, vb = qh.to(dev), kh.to(dev), vh.to(dev)
+    ex = tp.ShiftedKV(world, shift, causal, rank)
+    order = tp.shift_table(world, shift)
+    n_patch = sum(1 for s in order[rank] if not causal or tp.causal_relation(rank, int(s)) != "none")
+
+    def step():
+        return ex.run(qb, kb, vb, tp.cuda_patch, tp.cuda_merge)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        o, l = step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    max_s = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    value = flops * args.steps / max_s / 1e12
+
+    # end to end: this rank's blocks from pinned host memory, its O and LSE back
+    qp, kp, vp = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lh = torch.empty(l.shape, dtype=l.dtype, pin_memory=True)
+    e_steps = max(3, min(args.steps, 10))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        qb.copy_(qp, non_blocking=True)
+        kb.copy_(kp, non_blocking=True)
+        vb.copy_(vp, non_blocking=True)
+        o, l = step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(l, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    m.mercury_sync_status(stream)
+    if rank == 0:
+        h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) * world
+        d2h = (o.numel() * o.element_size() + l.numel() * l.element_size()) * world
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / args.steps, 4), "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)*%g, bf16)" % w["scale"],
+            "config": {"workload": args.workload, "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Skv": Skv, "d": d,
+                       "R": world, "shift": shift, "causal": bool(causal), "mode": "fused per step + merge",
+                       "parallelism": "shifted KV exchange over %d GPUs (NCCL point to point)" % world,
+                       "l2": "inputs larger than L2, no flush"},
+            "gpu_launches": args.steps * (n_patch + max(0, n_patch - 1)),
+            "e2e": {"value": round(flops * e_steps / e_s / 1e12, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e_steps},
+            "roofline": None, "cpu_baseline": None,
+            "note": "rank 0's line; the per-rank causal work is uneven (rank i runs i + 1 of the %d shards)"
+                    % world if causal else "rank 0's line",
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+
+
 def measure_gemm(m, dev, stream, peaks, peak_kind, reps: int = 10):
     """The shifted-shard GEMM (all-gather GEMM pattern) on its workload: TFLOP/s
     of mercury_gemm_shifted (2*M*N*K flop per call)."""
@@ -662,6 +775,9 @@ def main(argv=None):
     ap.add_argument("--no-secondary", action="store_true", help="do not time the GEMM and decode figures")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="do not time the CPU oracle")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi")
+    ap.add_argument("--dist-mode", choices=["shifted", "replicas"], default="shifted",
+                    help="with several GPUs: split the workload over them and exchange KV shards in the "
+                         "shifted order (default), or run independent replicas")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -673,6 +789,8 @@ def main(argv=None):
             ap.error("--gpus %d needs torchrun with %d processes" % (args.gpus, args.gpus))
     if args.impl == "reference":
         run_reference(args)
+    elif world > 1 and args.dist_mode == "shifted":
+        run_gpu_shifted(args)
     else:
         run_gpu(args)
 

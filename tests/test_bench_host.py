@@ -76,3 +76,22 @@ def test_reference_arm_nonzero_rank_does_nothing(monkeypatch, capsys):
 def bench_args():
     import argparse
     return argparse.Namespace(workload="mha_b1_h4_d64_s512_r4", steps=1, warmup=3)
+
+
+def test_shift_order_across_devices():
+    """With several GPUs the workload's nested order keeps its inner size when
+    that splits the GPUs into two or more groups; otherwise the flat order."""
+    assert bench.dist_shift_for(8, 4) == 4
+    assert bench.dist_shift_for(8, 2) == 2
+    assert bench.dist_shift_for(4, 4) == 1
+    assert bench.dist_shift_for(2, 4) == 1
+    assert bench.dist_shift_for(4, 1) == 1
+    assert bench.dist_shift_for(6, 4) == 1
+
+
+def test_local_blocks_tile_the_sequence():
+    import torch
+    t = torch.arange(2 * 3 * 16 * 4).view(2, 3, 16, 4)
+    parts = [bench.local_block(t, r, 4) for r in range(4)]
+    assert all(p.shape == (2, 3, 4, 4) and p.is_contiguous() for p in parts)
+    assert torch.equal(torch.cat(parts, dim=2), t)
