@@ -10,10 +10,15 @@
 // rank i at step j computes C[block i, shard order[i][j]] = A_i B_s.  The
 // result is C = A B, fp32, from bf16 inputs.
 //
-// Kernel: persistent, one CTA per SM walking output tiles of 256 x 256 in
-// step-major order (step j, rank i, then the tiles of that (rank, shard)
-// block), so the CTAs resident together share one A block and one B shard in
-// L2.  Warp 0: TMA producer (A tile 256 x 64 as two 128-row boxes, K-major;
+// Kernel: persistent, one CTA per SM walking output tiles of 256 x 256.  The
+// shift fixes which shard each rank reads at each step; on one GPU the order
+// in which the (rank, step) blocks run is free, since all R virtual ranks
+// share one L2.  Blocks run shard-major -- for each B shard s, the R ranks
+// that read it, in the order of the steps at which they do -- so a shard is
+// fetched into L2 once and its R readers follow each other (step-major order
+// fetched every shard and every A block again at every step).  Inside a block
+// the tiles along a row of C are adjacent, so the CTAs resident together
+// share the A rows too.  Warp 0: TMA producer (A tile 256 x 64 as two 128-row boxes, K-major;
 // B tile 64 x 256 as four 64-column boxes, N-major) into a 3-stage ring:
 // 64 KB per 1024 tensor cycles, two thirds of what 128 x 256 tiles pull from
 // L2 per FLOP.  Warp 1 (one elected lane) issues tcgen05.mma kind::f16, M = 128,
@@ -64,9 +69,9 @@ struct GemmParams {
     int KB;            // 64-wide K steps
     long long n_items;
     float *c;
+    unsigned char reader[kMaxR * kMaxR];  // reader[s*R + p]: the p-th rank to read shard s (by step, then rank)
     int c_v8;          // c is 32-byte aligned (N % 8 == 0 keeps every row so)
     unsigned long long wait_ns;
-    unsigned char order[kMaxR * kMaxR];
 };
 
 __device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, unsigned long long budget,
@@ -118,14 +123,15 @@ struct GTile {
     int m_end, n_end;  // rows / columns of the tile's (rank, shard) block end here
 };
 
-// Item idx (step-major): ct fastest, then rt, rank i, step j slowest.
+// Item idx (shard-major): ct fastest, then rt, then the shard's readers in
+// the order of their steps, shard s slowest.
 __device__ __forceinline__ GTile decode_gtile(const GemmParams &p, long long idx)
 {
     const int ct = (int)(idx % p.CT); idx /= p.CT;
     const int rt = (int)(idx % p.RT); idx /= p.RT;
-    const int i = (int)(idx % p.R); idx /= p.R;
-    const int j = (int)idx;
-    const int s = p.order[i * p.R + j];
+    const int pos = (int)(idx % p.R); idx /= p.R;
+    const int s = (int)idx;
+    const int i = p.reader[s * p.R + pos];
     GTile t;
     t.m0 = i * p.Mr + rt * kBM;
     t.n0 = s * p.Nr + ct * kBN;
@@ -401,8 +407,16 @@ int launch_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R
     p.c = c;
     p.c_v8 = ((uintptr_t)c % 32 == 0 && N % 8 == 0) ? 1 : 0;
     p.wait_ns = wait_ns;
-    for (int i = 0; i < R * R; ++i)
-        p.order[i] = (unsigned char)order[i];
+    // every rank reads every shard once (each row of the table is a
+    // permutation); a shard's readers go by the step at which they read it,
+    // ties (the unshifted order: all ranks at the same step) by rank
+    for (int s = 0; s < R; ++s) {
+        int n = 0;
+        for (int j = 0; j < R; ++j)
+            for (int i = 0; i < R; ++i)
+                if (order[i * R + j] == s)
+                    p.reader[s * R + n++] = (unsigned char)i;
+    }
     CUtensorMap ma, mb;
     // A is loaded as two 128-row boxes per stage, B as four 64-column boxes:
     // the boxes must add up to the bytes each stage's barrier expects
