@@ -64,6 +64,8 @@ struct AttnParams {
                              // 2 = drop the first "iteration done" arrive (kv_free)
     int out_bf16;            // fused calls only: O is written as bf16 ([B,Hq,Sq,d], 2 bytes)
     int out_v8;              // O's base is 32-byte aligned: rows are stored 32 bytes per lane
+    int o_tma;               // fp32 O: rows go out through shared memory and TMA tensor stores
+    long long o_rows;        // rows of the O tensor map (all slots)
     float *out;              // fused: out; partial: o_part
     float *lse;              // fused: lse; partial: lse_part
     long long out_elems;     // elements of out / o_part (all slots); checked build only
@@ -164,7 +166,11 @@ struct Smem {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = 2 * kQBytes;
     static constexpr int kOffV = kOffK + NK * kKVBytes;
-    static constexpr int kOffBar = kOffV + NV * kKVBytes;
+    // O staging for the epilogue's tensor stores: 32 rows x 32 fp32 (4 KB,
+    // 128-byte swizzle) per softmax warp
+    static constexpr int kStageBytes = 32 * 32 * 4;
+    static constexpr int kOffStage = kOffV + NV * kKVBytes;
+    static constexpr int kOffBar = kOffStage + 8 * kStageBytes;
     static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
     static constexpr int kNumBars = 1 + NK + NV + NE + 8 + 1;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem slot, abort flag
@@ -206,9 +212,11 @@ __device__ __forceinline__ int item_tiles(const AttnParams &p, const Item &it)
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
-                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV)
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmO)
 {
     using L = Smem<D, NK, NV>;
+    static_assert(L::kOffStage % 1024 == 0, "128-byte swizzled staging needs 1024-byte alignment");
     constexpr int NE = L::NE;
     constexpr int NBOX = D / 64;  // 128-byte swizzle columns per row
     // tensor-memory columns of S_t and O_t
@@ -708,49 +716,87 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             ++od;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
+            // When this warp's 32 rows are 32 consecutive rows of O (one head,
+            // all valid), each 32-column chunk goes through the warp's 4 KB of
+            // shared memory (lane = row, 128-byte swizzle: conflict-free) and
+            // one TMA tensor store, instead of 32 row-strided stores per
+            // instruction -- the epilogue sits between two work items.
+            const bool tma_rows = p.o_tma && p.g.Mq >= 32 && __all_sync(0xffffffffu, orow != nullptr);
+            if (tma_rows) {
+                const long long off0 = __shfl_sync(0xffffffffu, (long long)(orow - p.out), 0);
+                const int y0 = (int)(off0 / D);
+                uint8_t *stage = smem + L::kOffStage + (warp - 4) * L::kStageBytes;
+                const uint32_t srow = smem_u32(stage) + lane * 128;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld_x32(tO + c0, o);
-                // Each lane stores its own row; 32-byte stores (one whole sector
-                // per lane) need half the store instructions and L1 wavefronts
-                // of 16-byte ones, and this loop is bound by them.
-                if (orow && p.out_bf16) {
-                    // the row's bf16 elements sit at half the fp32 offset
-                    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + (orow - p.out) + c0;
-                    uint32_t w[16];
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + c0, o);
+                    if (lane == 0)
+                        bulk_wait_read_all();  // the previous store has read the staging rows
+                    __syncwarp();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                                  __uint_as_float(o[2 * e + 1]) * inv);
-                        w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(srow + ((c ^ (lane & 7)) << 4),
+                                     __float_as_uint(__uint_as_float(o[4 * c]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kChecked && (y0 < 0 || (long long)y0 + 32 > p.o_rows || c0 + 32 > D)) {
+                            record_bounds(0x504);
+                        } else {
+                            tma_store_2d(&tmO, stage, c0, y0);
+                            bulk_commit_group();
+                        }
                     }
-                    if (p.out_v8) {
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(tO + c0, o);
+                    // Each lane stores its own row; 32-byte stores (one whole sector
+                    // per lane) need half the store instructions and L1 wavefronts
+                    // of 16-byte ones, and this loop is bound by them.
+                    if (orow && p.out_bf16) {
+                        // the row's bf16 elements sit at half the fp32 offset
+                        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + (orow - p.out) + c0;
+                        uint32_t w[16];
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            st_global_v8(dst + 16 * c, w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3],
-                                         w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
-                    } else {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                        for (int e = 0; e < 16; ++e) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                                      __uint_as_float(o[2 * e + 1]) * inv);
+                            w[e] = *reinterpret_cast<uint32_t *>(&h2);
+                        }
+                        if (p.out_v8) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-                    }
-                } else if (orow) {
+                            for (int c = 0; c < 2; ++c)
+                                st_global_v8(dst + 16 * c, w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3],
+                                             w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
+                        } else {
+                            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * inv);
-                    if (p.out_v8) {
+                            for (int c = 0; c < 4; ++c)
+                                d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                        }
+                    } else if (orow) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            st_global_v8(orow + c0 + 8 * c, o[8 * c], o[8 * c + 1], o[8 * c + 2], o[8 * c + 3],
-                                         o[8 * c + 4], o[8 * c + 5], o[8 * c + 6], o[8 * c + 7]);
-                    } else {
-                        float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * inv);
+                        if (p.out_v8) {
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                                                 __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                            for (int c = 0; c < 4; ++c)
+                                st_global_v8(orow + c0 + 8 * c, o[8 * c], o[8 * c + 1], o[8 * c + 2], o[8 * c + 3],
+                                             o[8 * c + 4], o[8 * c + 5], o[8 * c + 6], o[8 * c + 7]);
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(orow + c0);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                dst[c] = make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                                                     __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                        }
                     }
                 }
             }
@@ -762,6 +808,9 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             if (lrow)
                 *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
+        // the O tensor stores this warp issued complete before the CTA leaves
+        if (lane == 0)
+            bulk_wait_all();
         tc_fence_before();
         named_barrier_sync(kExitBarrier, kThreads);
     }
@@ -787,6 +836,28 @@ EncodeFn get_encode_fn(char *msg, size_t msg_len)
     return fn;
 }
 
+// 2-D fp32 tensor [d1][d0] (d0 innermost), box {b0, b1}, 128-byte swizzle:
+// the epilogue's O stores.
+int encode_2d_f32(CUtensorMap *m, void *base, uint64_t d0, uint64_t d1, uint32_t b0, uint32_t b1, char *msg,
+                  size_t msg_len)
+{
+    EncodeFn fn = get_encode_fn(msg, msg_len);
+    if (!fn)
+        return MERCURY_ECUDA;
+    cuuint64_t dims[2] = {d0, d1};
+    cuuint64_t strides[1] = {d0 * 4};
+    cuuint32_t box[2] = {b0, b1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(msg, msg_len, "cuTensorMapEncodeTiled (O) failed (CUresult %d)", (int)r);
+        return MERCURY_ECUDA;
+    }
+    return MERCURY_OK;
+}
+
 // 3-D bf16 tensor [d2][d1][d0] (d0 innermost), 128-byte swizzle, zero fill.
 int encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
               uint32_t b1, uint32_t b2, char *msg, size_t msg_len)
@@ -810,7 +881,7 @@ int encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
 
 template <int D, int NK, int NV>
 int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                cudaStream_t stream, char *msg, size_t msg_len)
+                const CUtensorMap &mo, cudaStream_t stream, char *msg, size_t msg_len)
 {
     using L = Smem<D, NK, NV>;
     auto kern = attn_fwd_kernel<D, NK, NV>;
@@ -833,7 +904,7 @@ int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &m
     const long long grid = p.g.n_items < sms ? p.g.n_items : sms;
     if (grid < 1)
         return MERCURY_OK;
-    kern<<<(unsigned)grid, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv);
+    kern<<<(unsigned)grid, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv, mo);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         snprintf(msg, msg_len, "attention kernel launch: %s", cudaGetErrorString(e));
@@ -865,6 +936,10 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     const int slots = c.mode == kFused ? 1 : p.g.n_groups;
     p.out_elems = slots * p.slot_o;
     p.lse_elems = slots * p.slot_lse;
+    p.o_rows = slots * p.slot_lse;
+    // fp32 O goes out through TMA tensor stores (32 fp32 = 128 bytes per box
+    // row; every row starts 16-byte aligned since d is 64 or 128)
+    p.o_tma = (!c.out_bf16 && p.o_rows < 0x7fffffffLL) ? 1 : 0;
     p.wait_ns = c.wait_ns;
     const int R = c.R;
     for (int i = 0; i < R; ++i)
@@ -884,11 +959,15 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     if (rc == MERCURY_OK)
         rc = encode_3d(&mv, c.v, (uint64_t)c.d, (uint64_t)c.Skv, (uint64_t)c.B * c.Hkv, 64, kTileKeys, 1, msg,
                        msg_len);
+    CUtensorMap mo;
+    memset(&mo, 0, sizeof mo);
+    if (rc == MERCURY_OK && p.o_tma)
+        rc = encode_2d_f32(&mo, c.out, (uint64_t)c.d, (uint64_t)p.o_rows, 32, 32, msg, msg_len);
     if (rc == MERCURY_OK) {
         if (c.d == 128)
-            rc = launch_impl<128, 2, 2>(p, mq, mk, mv, stream, msg, msg_len);
+            rc = launch_impl<128, 2, 2>(p, mq, mk, mv, mo, stream, msg, msg_len);
         else
-            rc = launch_impl<64, 4, 4>(p, mq, mk, mv, stream, msg, msg_len);
+            rc = launch_impl<64, 4, 4>(p, mq, mk, mv, mo, stream, msg, msg_len);
     }
     return rc;
 }

@@ -15,6 +15,7 @@ already; it also passes alone in a fresh process (the first call does the
 per-device set-up, which loads the array's module).
 """
 import ctypes
+import gc
 
 import numpy as np
 import pytest
@@ -77,11 +78,18 @@ def test_noalloc_matches_sharded_and_oracle_two_calls(m, cfg):
         # the allocating entry point's result, taken before the bracket
         o_sh, l_sh = m.mercury_attn_sharded(qd, kd, vd, R, shift, causal)
         m.mercury_sync_status()
-        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-        rc = noalloc_call(m, qd, kd, vd, R, shift, causal, n_runs, out, lse)
-        assert rc == 0, m.lib.mercury_last_error()
-        m.mercury_sync_status()
-        free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        # no garbage collection inside the bracket: a collected cycle holding a
+        # CUDA tensor would change torch's count without any allocation here
+        gc.collect()
+        gc.disable()
+        try:
+            free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+            rc = noalloc_call(m, qd, kd, vd, R, shift, causal, n_runs, out, lse)
+            assert rc == 0, m.lib.mercury_last_error()
+            m.mercury_sync_status()
+            free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
         if call == 1:
             # the first call on a device may load the array's module; later
             # calls allocate nothing
