@@ -40,6 +40,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -57,6 +60,12 @@ namespace mercury {
 __device__ unsigned int g_err_word = 0;
 __device__ unsigned int g_err_site = 0;
 
+// Work-item counters for dynamically scheduled launches: each launch takes
+// the next slot (cycling) and zeroes it on its stream first, so launches on
+// different streams never share one.
+constexpr int kItemCounterSlots = 4096;
+__device__ unsigned int g_item_counters[kItemCounterSlots];
+
 struct AttnParams {
     Geom g;
     float scale_log2;        // log2(e) / sqrt(d)
@@ -73,6 +82,9 @@ struct AttnParams {
     long long slot_o;        // partial: elements between slots of o_part
     long long slot_lse;      // partial: elements between slots of lse_part
     unsigned long long wait_ns;
+    // Dynamic work items: the producer claims item gridDim.x + atomicAdd(*item_counter)
+    // after each CTA's first item (blockIdx.x); nullptr = static round robin.
+    unsigned int *item_counter;
     // fused, grouped: tab[i*R + j] = shard of rank i at step j;
     // per step: tab[i*R + s] = step (slot) at which rank i reads shard s.
     unsigned char tab[kMaxR * kMaxR];
@@ -81,6 +93,7 @@ struct AttnParams {
 namespace {
 
 constexpr int kThreads = 384;
+constexpr int kItemSlots = 4;  // work items published by the producer ahead of the other roles
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 2^8
@@ -172,8 +185,9 @@ struct Smem {
     static constexpr int kOffStage = kOffV + NV * kKVBytes;
     static constexpr int kOffBar = kOffStage + 8 * kStageBytes;
     static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
-    static constexpr int kNumBars = 1 + NK + NV + NE + 8 + 1;
-    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem slot, abort flag
+    static constexpr int kNumBars = 1 + NK + NV + NE + 8 + 1 + 2 * kItemSlots;
+    static constexpr int kOffRing = kOffBar + 8 * kNumBars;      // kItemSlots published item indices
+    static constexpr int kOffMisc = kOffRing + 8 * kItemSlots;  // tmem slot, abort flag
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -249,6 +263,11 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *o_full = p_full + 2;
     uint64_t *o_free = o_full + 2;  // O_t read out by the softmax warps
     uint64_t *mma_done = o_free + 2;  // every MMA the issuer issued has completed (exit)
+    // dynamic work items: item_full[s] = the producer published slot s;
+    // item_empty[s] = the MMA warp and the 8 softmax warps have read it
+    uint64_t *item_full = mma_done + 1;
+    uint64_t *item_empty = item_full + kItemSlots;
+    volatile long long *item_ring = (volatile long long *)(smem + L::kOffRing);
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -256,6 +275,27 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     const int lane = threadIdx.x % 32;
     const Ctl ctl{p.wait_ns, abort_flag};
     const long long n_items = p.g.n_items;
+    const bool dyn = p.item_counter != nullptr;
+    // Item k of this CTA on the consumer side: static round robin, or the
+    // index the producer published in ring slot k % kItemSlots; -1 past the
+    // end (or when the wait gave up: ok is then false).
+    auto take_item = [&](int k, bool &ok_, uint32_t site, int lane_) -> long long {
+        if (!dyn) {
+            const long long i = blockIdx.x + (long long)k * gridDim.x;
+            return i < n_items ? i : -1;
+        }
+        const int slot = k % kItemSlots;
+        const bool got = wait_phase(item_full + slot, (uint32_t)(k / kItemSlots) & 1u, ctl, site);
+        if (!__all_sync(0xffffffffu, got)) {
+            ok_ = false;
+            return -1;
+        }
+        const long long i = item_ring[slot];
+        __syncwarp();
+        if (lane_ == 0)
+            mbar_arrive(item_empty + slot);
+        return i;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -272,6 +312,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             mbar_init(o_free + t, 4);  // one arrive per softmax warp
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(item_full + i, 1);
+            mbar_init(item_empty + i, 9);  // the MMA warp and the 8 softmax warps
+        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -297,7 +341,26 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             int g = 0;  // tile-iterations issued so far by this CTA
             int nq = 0, nk = 0, nv = 0;  // Q, K and V loads issued (their barriers' phases)
             bool ok = true;
-            for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                // this CTA's item k: round robin, or (dynamic) claimed from the
+                // launch's counter after the first and published to the other roles
+                long long idx = blockIdx.x + (long long)k * gridDim.x;
+                if (dyn && k > 0)
+                    idx = (long long)gridDim.x + atomicAdd(p.item_counter, 1u);
+                if (idx >= n_items)
+                    idx = -1;
+                if (dyn) {
+                    const int slot = k % kItemSlots;
+                    if (k >= kItemSlots &&
+                        !wait_phase(item_empty + slot, (uint32_t)(k / kItemSlots - 1) & 1u, ctl, 0x104)) {
+                        ok = false;
+                        break;
+                    }
+                    item_ring[slot] = idx;
+                    mbar_arrive(item_full + slot);
+                }
+                if (idx < 0)
+                    break;
                 const Item it = decode_item(p.g, idx);
                 const int ntot = item_tiles(p, it);
                 if (ntot == 0)
@@ -425,7 +488,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             int sp[2] = {0, 0};         // S_t / P_t phases so far, per tile
             int od[2] = {0, 0};         // O_t finalisations so far, per tile
             bool ok = true;
-            for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const long long idx = take_item(k, ok, 0x206, lane);
+                if (idx < 0)
+                    break;
                 const Item it = decode_item(p.g, idx);
                 const int ntot = item_tiles(p, it);
                 if (ntot == 0)
@@ -527,7 +593,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         int sp = 0;  // S_t / P_t phases of this tile so far
         int od = 0;  // O_t finalisations of this tile so far
         bool ok = true;
-        for (long long idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const long long idx = take_item(k, ok, 0x303, lane);
+            if (idx < 0)
+                break;
             const Item it = decode_item(p.g, idx);
             const int ntot = item_tiles(p, it);
             const int ntile = it.t[1].valid ? 2 : 1;
@@ -879,8 +948,47 @@ int encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
     return MERCURY_OK;
 }
 
+// A zeroed work-item counter for one launch on `stream`: the next slot of
+// g_item_counters (cycling through kItemCounterSlots), cleared by a memset
+// ordered before the launch.  The array's device address is looked up once
+// per device.
+int claim_item_counter(cudaStream_t stream, unsigned int **out, char *msg, size_t msg_len)
+{
+    static std::mutex mu;
+    static unsigned int *base[64] = {};
+    static std::atomic<unsigned int> next{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        snprintf(msg, msg_len, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    unsigned int *b = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!base[dev]) {
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_item_counters);
+            if (e != cudaSuccess || !ptr) {
+                snprintf(msg, msg_len, "cudaGetSymbolAddress(item counters): %s", cudaGetErrorString(e));
+                return MERCURY_ECUDA;
+            }
+            base[dev] = (unsigned int *)ptr;
+        }
+        b = base[dev];
+    }
+    unsigned int *c = b + (next.fetch_add(1u, std::memory_order_relaxed) % kItemCounterSlots);
+    e = cudaMemsetAsync(c, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) {
+        snprintf(msg, msg_len, "clearing the work-item counter: %s", cudaGetErrorString(e));
+        return MERCURY_ECUDA;
+    }
+    *out = c;
+    return MERCURY_OK;
+}
+
 template <int D, int NK, int NV>
-int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+int launch_impl(AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const CUtensorMap &mo, cudaStream_t stream, char *msg, size_t msg_len)
 {
     using L = Smem<D, NK, NV>;
@@ -904,6 +1012,17 @@ int launch_impl(const AttnParams &p, const CUtensorMap &mq, const CUtensorMap &m
     const long long grid = p.g.n_items < sms ? p.g.n_items : sms;
     if (grid < 1)
         return MERCURY_OK;
+    // Causal items differ in length (a block sees up to its diagonal): with
+    // more items than CTAs, each CTA takes its next item when it is free
+    // (items stay in their heaviest-first, head-by-head order), instead of
+    // every grid-th one -- round robin left the busiest CTA 8-11 % above the
+    // mean on 8K-32K causal shapes.
+    p.item_counter = nullptr;
+    if (p.g.causal && p.g.n_items > grid) {
+        rc = claim_item_counter(stream, &p.item_counter, msg, msg_len);
+        if (rc != MERCURY_OK)
+            return rc;
+    }
     kern<<<(unsigned)grid, kThreads, L::kAlloc, stream>>>(p, mq, mk, mv, mo);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -201,9 +201,54 @@ def test_sharded_bf16_output(m, cfg, groups, monkeypatch):
     assert_close(o16.float().cpu().numpy(), l16.cpu().numpy(), o_ref, l_ref, "bf16 out")
 
 
+# Causal shapes with more work items than the GPU has SMs: each CTA claims its
+# next item from the launch's counter when it is free (dynamic scheduling).
+DYNAMIC = [
+    # B, Hq, Hkv, Sq, Skv, d, R, shift, causal
+    (1, 32, 8, 4096, 4096, 128, 8, 1, True),    # 512 items
+    (2, 16, 16, 2048, 2048, 64, 4, 2, True),    # MHA row pairs, nested 2x2, 256 items
+]
+
+
+@pytest.mark.parametrize("cfg", DYNAMIC, ids=lambda c: "x".join(map(str, c)))
+def test_dynamic_items_all_rows(m, cfg):
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    info = m.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, 0)
+    assert info["n_items"] > torch.cuda.get_device_properties(0).multi_processor_count
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 3)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "fused, dynamic items")
+    _, _, out, lse = run_partial_merge(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "per-step partials, dynamic items")
+
+
+def test_dynamic_items_on_two_streams_at_once(m):
+    """Two causal calls in flight on two streams take different work-item
+    counters: both results are right."""
+    cfg = (1, 32, 8, 4096, 4096, 128, 8, 1, True)
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    ins = [make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=s) for s in (71, 72)]
+    dev = [tuple(x.cuda() for x in t) for t in ins]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    torch.cuda.synchronize()
+    for (qd, kd, vd), st in zip(dev, streams):
+        out = torch.empty((B, Hq, Sq, d), device="cuda")
+        lse = torch.empty((B, Hq, Sq), device="cuda")
+        m.mercury_attn_sharded(qd, kd, vd, R, shift, causal, out, lse, stream=st)
+        outs.append((out, lse))
+    torch.cuda.synchronize()
+    m.mercury_sync_status()
+    for (q, k, v), (out, lse) in zip(ins, outs):
+        o_ref, l_ref = oracle.attn(q, k, v, causal)
+        assert_close(out.cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, "concurrent stream")
+
+
 @pytest.mark.parametrize("cfg", [(1, 8, 2, 2048, 2048, 128, 4, 1, True),     # fused schedule
-                                 (1, 8, 1, 128, 16384, 128, 8, 1, False)],  # split-KV + merge
-                         ids=["fused", "split"])
+                                 (1, 8, 1, 128, 16384, 128, 8, 1, False),   # split-KV + merge
+                                 (1, 32, 8, 4096, 4096, 128, 8, 1, True)],  # dynamic work items
+                         ids=["fused", "split", "dynamic"])
 def test_cuda_graph_capture_and_replay(m, cfg):
     """The calls are stream-ordered and capturable: capture once (after a
     warm-up call on the same stream), replay with new inputs copied in place."""
