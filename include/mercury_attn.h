@@ -387,10 +387,11 @@ MERCURY_API int mercury_measure_cost_profile(mercury_cost_profile *prof, void *s
  * divides Sq); every distinct n_runs in 1..R.  Drops those whose hbm_bytes
  * exceed budget_bytes (budget_bytes <= 0: no limit) and estimates the rest:
  * every work item costs item_us plus its K/V tiles times tile_us (tile1_us
- * for one query tile), items go to n_sms CTAs round robin in launch order,
- * and the attention launch costs launch_us plus the larger of the busiest
- * CTA's sum and its least memory traffic (q, k, v read once, its outputs
- * written once) at hbm_gbs; when n_runs > 1 a second launch and the merge's
+ * for one query tile), items go to n_sms CTAs round robin in launch order
+ * (in a causal launch with more items than CTAs, as the kernel does: each to
+ * the CTA free earliest), and the attention launch costs launch_us plus the
+ * larger of the busiest CTA's sum and its least memory traffic (q, k, v read
+ * once, its outputs written once) at hbm_gbs; when n_runs > 1 a second launch and the merge's
  * bytes at merge_gbs are added.
  * Writes the min(count, max_plans) fastest candidates to plans[], fastest
  * first (ties: fewer hbm_bytes, then Rq == R, then smaller R, then fewer

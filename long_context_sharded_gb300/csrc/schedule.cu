@@ -18,6 +18,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string>
+#include <queue>
 #include <vector>
 
 #include "internal.h"
@@ -73,15 +74,43 @@ double item_cost(const Geom &g, const Item &it, const int *order, const mercury_
     return p.item_us + (double)item_tiles(g, it, order) * per_tile;
 }
 
-// Device time of one launch of geometry g: items go round robin to
-// min(n_items, n_sms) persistent CTAs in launch order; the launch lasts as
-// long as its busiest CTA, plus the launch cost.
+// Least HBM time of one launch: q, k, v read once; O and LSE (or every
+// slot's partials) written once.
+double traffic_floor_us(const Geom &g, const mercury_cost_profile &p)
+{
+    const double rows = (double)g.B * g.Hq * g.Sq;
+    const double in = rows * g.d * 2.0 + 2.0 * g.B * g.Hkv * (double)g.Skv * g.d * 2.0;
+    const double outb = (g.partial == kFused ? 1.0 : (double)g.n_groups) * rows * (g.d + 1) * 4.0;
+    return (in + outb) / (p.hbm_gbs * 1e3);
+}
+
+// Device time of one launch of geometry g on min(n_items, n_sms) persistent
+// CTAs: the launch lasts as long as its busiest CTA, plus the launch cost.
+// Items go round robin in launch order -- except in causal launches with
+// more items than CTAs, where each CTA claims the next item when it becomes
+// free (the kernel's dynamic scheduling): CTA i takes item i first, then each
+// item goes to the CTA that is free earliest (ties: the lower index).
 double launch_estimate(const Geom &g, const int *order, const mercury_cost_profile &p)
 {
     const long long n = g.n_items;
     if (n <= 0)
         return p.launch_us;
     const long long grid = std::min<long long>(n, p.n_sms);
+    if (g.causal && n > grid) {
+        using Slot = std::pair<double, long long>;  // (busy until, CTA)
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+        for (long long c = 0; c < grid; ++c)
+            free_at.push(Slot(0.0, c));
+        double last = 0.0;
+        for (long long i = 0; i < n; ++i) {
+            Slot s = free_at.top();
+            free_at.pop();
+            s.first += item_cost(g, decode_item(g, i), order, p);
+            last = std::max(last, s.first);
+            free_at.push(s);
+        }
+        return p.launch_us + std::max(last, traffic_floor_us(g, p));
+    }
     std::vector<double> diff(grid + 1, 0.0);
     double everyone = 0.0;
     // Otherwise items sharing (row tile, rank, slot) sit in runs of NHP*Hkv*B
@@ -136,13 +165,7 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
         run += diff[c];
         best = std::max(best, run);
     }
-    // least traffic: q, k, v read once; O and LSE (or every slot's partials)
-    // written once
-    const double rows = (double)g.B * g.Hq * g.Sq;
-    const double in = rows * g.d * 2.0 + 2.0 * g.B * g.Hkv * (double)g.Skv * g.d * 2.0;
-    const double outb = (g.partial == kFused ? 1.0 : (double)g.n_groups) * rows * (g.d + 1) * 4.0;
-    const double floor_us = (in + outb) / (p.hbm_gbs * 1e3);
-    return p.launch_us + std::max(everyone + best, floor_us);
+    return p.launch_us + std::max(everyone + best, traffic_floor_us(g, p));
 }
 
 int check_profile(const mercury_cost_profile *p)

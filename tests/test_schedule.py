@@ -67,6 +67,7 @@ SHAPES = [
     (2, 2, 2, 384, 384, 128, True, 3, 1),
     (1, 8, 1, 128, 4096, 128, False, 8, 1),
     (1, 6, 2, 256, 512, 64, True, 4, 0),     # three head tiles per KV group: odd head pairs
+    (1, 32, 8, 2048, 2048, 128, True, 8, 1), # causal, more items than SMs: claimed dynamically
 ]
 
 
@@ -119,7 +120,10 @@ def test_budget_filter_and_pareto(m, shape):
 
 
 def simulate(m, oracle, shape, runs, prof):
-    """Round-robin simulation of one candidate with Rq = R, item by item."""
+    """Simulation of one candidate with Rq = R, item by item: round robin, or,
+    for a causal launch with more items than CTAs, each item to the CTA that
+    is free earliest (the kernel claims items dynamically there)."""
+    import heapq
     B, Hq, Hkv, Sq, Skv, d, causal, R, shift = shape
     mode = 0 if runs == 1 else (1 if runs == R else runs)
     info = m.mercury_work_decomposition(B, Hq, Hkv, Sq, Skv, d, R, causal, mode)
@@ -129,6 +133,8 @@ def simulate(m, oracle, shape, runs, prof):
     spg = -(-R // runs)
     grid = min(n_items, prof.n_sms)
     busy = [0.0] * grid
+    dynamic = causal and n_items > grid
+    heap = [(0.0, c) for c in range(grid)]
     for item in range(n_items):
         rows, slot = m.mercury_work_item_rows(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, mode, item)
         qs = [r % Sq for r in rows]
@@ -147,7 +153,13 @@ def simulate(m, oracle, shape, runs, prof):
             s = order[rank][j]
             lo, hi = s * Bk, min(s * Bk + Bk, kv_end)
             tiles += max(0, -(-(hi - lo) // 128))
-        busy[item % grid] += prof.item_us + tiles * prof.tile_us
+        cost = prof.item_us + tiles * prof.tile_us
+        if dynamic:
+            until, cta = heapq.heappop(heap)
+            heapq.heappush(heap, (until + cost, cta))
+            busy[cta] = until + cost
+        else:
+            busy[item % grid] += cost
     t = prof.launch_us + max(busy)
     if runs > 1:
         rows_total = B * Hq * Sq
