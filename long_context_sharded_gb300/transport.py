@@ -131,7 +131,7 @@ class ShiftedKV:
     Messages are sent as bytes, so any dtype travels (gloo has no bf16).
     """
 
-    def __init__(self, R: int, shift: int, causal: bool, rank: int, group=None):
+    def __init__(self, R: int, shift: int, causal: bool, rank: int, group=None, record_checksums: bool = False):
         import torch.distributed as dist
         self.dist = dist
         self.R, self.shift, self.causal, self.rank, self.group = R, shift, bool(causal), rank, group
@@ -140,7 +140,11 @@ class ShiftedKV:
         if dist.get_world_size(group) != R:
             raise ValueError("the process group must have R = %d ranks" % R)
         self.received: List[int] = []      # shard index used at each step
-        self.checksums: List[float] = []   # sum of the shard's elements at each step (for checks)
+        # Sum of each step's shard (record_checksums=True, for checks only: it
+        # reads the shard back to the host every step, which serialises the
+        # exchange with the compute).
+        self.record_checksums = record_checksums
+        self.checksums: List[float] = []
 
     def _global(self, r: int) -> int:
         return r if self.group is None else self.dist.get_global_rank(self.group, r)
@@ -176,7 +180,8 @@ class ShiftedKV:
             works = self._start(j + 1, own, cur, nxt) if j + 1 < self.R else []
             s = int(self.order[self.rank, j])
             self.received.append(s)
-            self.checksums.append(float(cur.double().sum()))
+            if self.record_checksums:
+                self.checksums.append(float(cur.double().sum()))
             rel = causal_relation(self.rank, s) if self.causal else "full"
             if rel != "none":
                 part = patch(q, cur[0], cur[1], rel)

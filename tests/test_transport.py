@@ -140,7 +140,7 @@ def _worker(rank, world, port, cfg, form, q_out):
         ks = k[:, :, rank * Bq:(rank + 1) * Bq].contiguous()
         vs = v[:, :, rank * Bq:(rank + 1) * Bq].contiguous()
         if form == "kv":
-            ex = tp.ShiftedKV(R, shift, causal, rank)
+            ex = tp.ShiftedKV(R, shift, causal, rank, record_checksums=True)
             o, l = ex.run(qi, ks, vs, _oracle_patch, _oracle_merge)
             true_sums = [float(torch.stack([k[:, :, s * Bq:(s + 1) * Bq], v[:, :, s * Bq:(s + 1) * Bq]])
                                .double().sum()) for s in ex.received]
