@@ -95,3 +95,26 @@ def test_local_blocks_tile_the_sequence():
     parts = [bench.local_block(t, r, 4) for r in range(4)]
     assert all(p.shape == (2, 3, 4, 4) and p.is_contiguous() for p in parts)
     assert torch.equal(torch.cat(parts, dim=2), t)
+
+
+def test_clock_normalised_ceiling():
+    """8192 FLOP/cycle/SM x SMs x MHz: 152 SMs at 2070 MHz is 2577.5 TFLOP/s."""
+    assert bench.clock_peak_tflops(152, 2070) == pytest.approx(8192 * 152 * 2070e6 / 1e12)
+    assert bench.clock_peak_tflops(152, 2070) == pytest.approx(2577.5, abs=0.1)
+    assert bench.clock_peak_tflops(152, None) is None
+
+
+def test_launches_per_call_follows_the_library_schedule(monkeypatch):
+    """The bench's launch count per mercury_attn_sharded call mirrors the
+    library's run-count choice: one launch for the fused workloads, attention
+    plus merge when the chooser splits (the 2M-token chunk)."""
+    from long_context_sharded_gb300 import build
+    build.build()
+    from long_context_sharded_gb300 import mercury as m
+    from long_context_sharded_gb300.workloads import WORKLOADS
+    monkeypatch.delenv("MERCURY_SPLIT_GROUPS", raising=False)
+    assert bench.launches_per_call(m, WORKLOADS["gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4"], 152) == 1
+    assert bench.launches_per_call(m, WORKLOADS["gqa_b1_hq32_hkv8_d128_s32k_causal_r8"], 152) == 1
+    assert bench.launches_per_call(m, WORKLOADS["mqa_b1_hq8_hkv1_d128_sq2k_skv2m_r64_merge"], 152) == 2
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "1")
+    assert bench.launches_per_call(m, WORKLOADS["mqa_b1_hq8_hkv1_d128_sq2k_skv2m_r64_merge"], 152) == 1
