@@ -171,6 +171,27 @@ COVERAGE = [
 ]
 
 
+def _random_coverage_shapes(n, seed):
+    """Seeded shapes within the call's contract (head packing, ragged blocks and
+    shards, GQA groups, causal with Sq <= Skv, every shift form)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        R = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+        Hkv = int(rng.choice([1, 2, 3]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        Sq = R * int(rng.integers(1, 80))
+        Skv = Sq if rng.random() < 0.5 else R * int(rng.integers(1, 120))
+        causal = int(rng.random() < 0.5 and Sq <= Skv)
+        shifts = [0, 1] + [k for k in range(2, R) if R % k == 0]
+        out.append((int(rng.choice([1, 2])), Hkv * G, Hkv, Sq, Skv, int(rng.choice([64, 128])), R,
+                    int(rng.choice(shifts)), causal))
+    return out
+
+
+COVERAGE += _random_coverage_shapes(10, 7)
+
+
 @pytest.mark.parametrize("cfg", COVERAGE)
 @pytest.mark.parametrize("mode", [0, 1, 2, 3, 5])
 def test_work_items_cover_each_output_once(m, cfg, mode):

@@ -540,3 +540,42 @@ def test_workload_mqa_2m_merge(m):
 @pytest.mark.slow
 def test_workload_gqa_128k_causal_nested(m):
     _run_workload(m, "gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4", check_cross=True)
+
+
+# ------------------------------------------------------ randomised shapes
+
+def _random_shapes(n, seed):
+    """Seeded shapes within the call's contract: d 64 or 128, GQA group 1-8,
+    R dividing both lengths, lengths that are not multiples of the 128-row
+    tiles, causal only with Sq <= Skv, every shift form R admits."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        d = int(rng.choice([64, 128]))
+        Hkv = int(rng.choice([1, 2, 3]))
+        G = int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.choice([1, 2]))
+        R = int(rng.choice([1, 2, 3, 4, 6, 8]))
+        Sq = R * int(rng.integers(8, 160))
+        Skv = Sq if rng.random() < 0.5 else R * int(rng.integers(8, 320))
+        causal = bool(rng.random() < 0.5) and Sq <= Skv
+        shifts = [0, 1] + [k for k in range(2, R) if R % k == 0]
+        shift = int(rng.choice(shifts))
+        out.append((B, Hkv * G, Hkv, Sq, Skv, d, R, shift, causal))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_shapes(12, 2026), ids=lambda c: "x".join(map(str, c)))
+def test_random_shapes_all_paths(m, cfg):
+    """Fused, per-step partials + merge and bf16 O on a seeded random shape,
+    every row against the oracle."""
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 11)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "fused")
+    _, _, out, lse = run_partial_merge(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "partials + merge")
+    o16, l16 = m.mercury_attn_sharded_bf16(q.cuda(), k.cuda(), v.cuda(), R, shift, causal)
+    m.mercury_sync_status()
+    assert_close(o16.float().cpu().numpy(), l16.cpu().numpy(), o_ref, l_ref, "bf16 O")
