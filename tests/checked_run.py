@@ -47,8 +47,26 @@ def close(o, l, o_ref, l_ref, what):
         raise SystemExit("%s: O max %.3g mean %.3g" % (what, err.max(), err.mean()))
 
 
+def compare_with_normal_build(path):
+    """Bit-identical to the normal build: the checks add branches, no arithmetic."""
+    ref = np.load(path)
+    n = 0
+    for i, cfg in enumerate(SHAPES):
+        B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+        q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]))
+        out, lse = m.mercury_attn_sharded(q.cuda(), k.cuda(), v.cuda(), R, shift, causal)
+        m.mercury_sync_status()
+        if not (np.array_equal(out.cpu().numpy(), ref["o%d" % i]) and
+                np.array_equal(lse.cpu().numpy(), ref["l%d" % i])):
+            raise SystemExit("checked and normal builds differ on %s" % (cfg,))
+        n += 1
+    return n
+
+
 def main():
     assert m.CHECKED, "MERCURY_CHECKED_BUILD=1 must select the checked library"
+    if len(sys.argv) > 1:
+        print("checked build: bit-identical to the normal build on %d shapes" % compare_with_normal_build(sys.argv[1]))
     n = 0
     for cfg in SHAPES:
         B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
