@@ -36,6 +36,12 @@
  *     error word and return early; that status is reported by
  *     mercury_sync_status().  With env MERCURY_SYNC_CHECK=1 every compute
  *     call synchronises its stream and returns the status itself.
+ *   - Causal calls with more work items than the GPU has SMs let each CTA
+ *     claim its next item from a counter: one of a fixed set of 4-byte slots
+ *     in the library's module, taken in turn per launch and cleared by a
+ *     memset on the call's stream (nothing is allocated; calls on different
+ *     streams use different slots).  The first such call on a device looks
+ *     up the slots' device address; make it before any stream capture.
  *   - Test hook (env MERCURY_FAULT, unset in normal use): drop_p_arrive or
  *     drop_kv_free makes the attention kernel withhold one internal arrive,
  *     so the MMA issuer's or the TMA producer's bounded wait runs out and the
