@@ -185,7 +185,7 @@ struct Smem {
     static constexpr int kOffStage = kOffV + NV * kKVBytes;
     static constexpr int kOffBar = kOffStage + 8 * kStageBytes;
     static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
-    static constexpr int kNumBars = 1 + NK + NV + NE + 8 + 1 + 2 * kItemSlots;
+    static constexpr int kNumBars = 2 + NK + NV + NE + 8 + 1 + 2 * kItemSlots;
     static constexpr int kOffRing = kOffBar + 8 * kNumBars;      // kItemSlots published item indices
     static constexpr int kOffMisc = kOffRing + 8 * kItemSlots;  // tmem slot, abort flag
     static constexpr int kBytes = kOffMisc + 16;
@@ -248,8 +248,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint8_t *sK = smem + L::kOffK;
     uint8_t *sV = smem + L::kOffV;
     uint64_t *bars = (uint64_t *)(smem + L::kOffBar);
-    uint64_t *q_full = bars;
-    uint64_t *k_full = q_full + 1;
+    uint64_t *q_full = bars;  // [2]: Q tile t of the current item has landed
+    uint64_t *k_full = q_full + 2;
     uint64_t *v_full = k_full + NK;
     // kv_free[g % NE], phase g / NE: the CTA's tile-iteration g (counted across
     // its items) is done -- S of the item's last tile is computed, so K(g) and
@@ -299,6 +299,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_full + 1, 1);
         for (int i = 0; i < NK; ++i)
             mbar_init(k_full + i, 1);
         for (int i = 0; i < NV; ++i)
@@ -339,7 +340,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             int g = 0;  // tile-iterations issued so far by this CTA
-            int nq = 0, nk = 0, nv = 0;  // Q, K and V loads issued (their barriers' phases)
+            int nq0 = 0, nq1 = 0, nk = 0, nv = 0;  // Q tile 0 / 1, K and V loads issued (barrier phases)
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 // this CTA's item k: round robin, or (dynamic) claimed from the
@@ -386,12 +387,15 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                         break;
                     }
                 }
-                mbar_arrive_expect_tx(q_full, (uint32_t)(ntile * L::kQBytes));
-                for (int t = 0; t < ntile; ++t)
-                    for (int c = 0; c < NBOX; ++c)
-                        tma_load_3d(sQ + t * L::kQBytes + c * L::kBoxBytes, &tmQ, q_full, c * 64,
-                                    it.t[t].q0, it.b * p.g.Hq + it.t[t].h0);
-                ++nq;
+                // Q tile 0 now and tile 1 right after the item's first K tile:
+                // the item's first Q K^T then waits for one Q tile and one K tile
+                // rather than both Q tiles ahead of the K tile
+                mbar_arrive_expect_tx(q_full, (uint32_t)L::kQBytes);
+                for (int c = 0; c < NBOX; ++c)
+                    tma_load_3d(sQ + c * L::kBoxBytes, &tmQ, q_full, c * 64, it.t[0].q0,
+                                it.b * p.g.Hq + it.t[0].h0);
+                ++nq0;
+                bool q1_pending = ntile == 2;
                 const int bkv = it.b * p.g.Hkv + it.hkv;
                 const int nsteps = item_steps(p.g, it);
                 for (int st = 0; st < nsteps && ok; ++st) {
@@ -418,6 +422,14 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             tma_load_3d(sK + sk * L::kKVBytes + c * L::kBoxBytes, &tmK, k_full + sk, c * 64,
                                         k0, bkv);
                         ++nk;
+                        if (q1_pending) {
+                            mbar_arrive_expect_tx(q_full + 1, (uint32_t)L::kQBytes);
+                            for (int c = 0; c < NBOX; ++c)
+                                tma_load_3d(sQ + L::kQBytes + c * L::kBoxBytes, &tmQ, q_full + 1, c * 64,
+                                            it.t[1].q0, it.b * p.g.Hq + it.t[1].h0);
+                            ++nq1;
+                            q1_pending = false;
+                        }
                         // stage g % NV held V(g - NV): free once iteration g - NV + 1 is done
                         const int ev = g - NV + 1;
                         if (g >= NV && !wait_phase(kv_free + ev % NE, (ev / NE) & 1, ctl, 0x102)) {
@@ -447,8 +459,10 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     const int last = nv - 1 - ((nv - 1 - s) % NV);
                     drain_phase(v_full + s, (last / NV) & 1, ctl, 0x112);
                 }
-            if (nq > 0)
-                drain_phase(q_full, (nq - 1) & 1, ctl, 0x113);
+            if (nq0 > 0)
+                drain_phase(q_full, (nq0 - 1) & 1, ctl, 0x113);
+            if (nq1 > 0)
+                drain_phase(q_full + 1, (nq1 - 1) & 1, ctl, 0x114);
         } else if (warp == 1) {
             // --------------------------------------------------- MMA issuer
             // The whole warp runs this loop (its waits and descriptor
@@ -484,7 +498,7 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                             kIdescPV, (acc_in || kk > 0) ? 1u : 0u, leader);
             };
             int g = 0;                  // tile-iterations of this CTA so far
-            int nq = 0;                 // items with work so far (q_full phases)
+            int nq0 = 0, nq1 = 0;       // Q tile 0 / tile 1 loads consumed (q_full phases)
             int sp[2] = {0, 0};         // S_t / P_t phases so far, per tile
             int od[2] = {0, 0};         // O_t finalisations so far, per tile
             bool ok = true;
@@ -497,8 +511,8 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                 if (ntot == 0)
                     continue;
                 const int ntile = it.t[1].valid ? 2 : 1;
-                ok = wait_phase(q_full, nq & 1, ctl, 0x201);
-                ++nq;
+                ok = wait_phase(q_full, nq0 & 1, ctl, 0x201);
+                ++nq0;
                 tc_fence_after();
                 // iteration n issues P.V of n-1 (n >= 1) and Q K^T of n (n < ntot)
                 for (int n = 0; n <= ntot && ok; ++n) {
@@ -513,8 +527,17 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     if (n == 0) {
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            if (t >= ntile)
+                            if (t >= ntile || !ok)
                                 break;
+                            if (t == 1) {
+                                // tile 1's Q follows the item's first K tile
+                                if (!wait_phase(q_full + 1, nq1 & 1, ctl, 0x208)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ++nq1;
+                                tc_fence_after();
+                            }
                             issue_qk(t, sk);
                             umma_commit_w(s_full + t, leader);
                             ++sp[t];
