@@ -94,6 +94,19 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kItemSlots = 4;  // work items published by the producer ahead of the other roles
+
+// A work item as the producer publishes it to the MMA and softmax warps:
+// decoded once, with its number of KV tiles, so that no consumer spends its
+// way from one item to the next on the index arithmetic (a few thousand
+// cycles of 64-bit division and a walk over the item's steps, measured on
+// the item boundary).  has == 0 ends the CTA's work.
+struct alignas(16) ItemSlot {
+    int has;
+    int ntot;   // KV tiles of the item's whole sequence
+    Item it;
+    int pad;
+};
+static_assert(sizeof(ItemSlot) == 64, "one 64-byte ring entry per item");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 2^8
@@ -186,8 +199,8 @@ struct Smem {
     static constexpr int kOffBar = kOffStage + 8 * kStageBytes;
     static constexpr int NE = NK > NV ? NK : NV;  // ring of "iteration done" events
     static constexpr int kNumBars = 2 + NK + NV + NE + 8 + 1 + 2 * kItemSlots;
-    static constexpr int kOffRing = kOffBar + 8 * kNumBars;      // kItemSlots published item indices
-    static constexpr int kOffMisc = kOffRing + 8 * kItemSlots;  // tmem slot, abort flag
+    static constexpr int kOffRing = (kOffBar + 8 * kNumBars + 15) / 16 * 16;  // kItemSlots published items
+    static constexpr int kOffMisc = kOffRing + (int)sizeof(ItemSlot) * kItemSlots;  // tmem slot, abort flag
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -263,11 +276,11 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     uint64_t *o_full = p_full + 2;
     uint64_t *o_free = o_full + 2;  // O_t read out by the softmax warps
     uint64_t *mma_done = o_free + 2;  // every MMA the issuer issued has completed (exit)
-    // dynamic work items: item_full[s] = the producer published slot s;
+    // work items: item_full[s] = the producer published ring slot s;
     // item_empty[s] = the MMA warp and the 8 softmax warps have read it
     uint64_t *item_full = mma_done + 1;
     uint64_t *item_empty = item_full + kItemSlots;
-    volatile long long *item_ring = (volatile long long *)(smem + L::kOffRing);
+    ItemSlot *item_ring = (ItemSlot *)(smem + L::kOffRing);
     uint32_t *tmem_slot = (uint32_t *)(smem + L::kOffMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
@@ -276,25 +289,21 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
     const Ctl ctl{p.wait_ns, abort_flag};
     const long long n_items = p.g.n_items;
     const bool dyn = p.item_counter != nullptr;
-    // Item k of this CTA on the consumer side: static round robin, or the
-    // index the producer published in ring slot k % kItemSlots; -1 past the
-    // end (or when the wait gave up: ok is then false).
-    auto take_item = [&](int k, bool &ok_, uint32_t site, int lane_) -> long long {
-        if (!dyn) {
-            const long long i = blockIdx.x + (long long)k * gridDim.x;
-            return i < n_items ? i : -1;
-        }
+    // Item k of this CTA on the consumer side, as the producer published it
+    // in ring slot k % kItemSlots.  false past the end of the CTA's work, or
+    // when the wait gave up (ok_ is then false).
+    auto take_item = [&](int k, bool &ok_, uint32_t site, int lane_, ItemSlot &out) -> bool {
         const int slot = k % kItemSlots;
         const bool got = wait_phase(item_full + slot, (uint32_t)(k / kItemSlots) & 1u, ctl, site);
         if (!__all_sync(0xffffffffu, got)) {
             ok_ = false;
-            return -1;
+            return false;
         }
-        const long long i = item_ring[slot];
+        out = item_ring[slot];
         __syncwarp();
         if (lane_ == 0)
             mbar_arrive(item_empty + slot);
-        return i;
+        return out.has != 0;
     };
 
     if (threadIdx.x == 0) {
@@ -350,20 +359,25 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
                     idx = (long long)gridDim.x + atomicAdd(p.item_counter, 1u);
                 if (idx >= n_items)
                     idx = -1;
-                if (dyn) {
-                    const int slot = k % kItemSlots;
-                    if (k >= kItemSlots &&
-                        !wait_phase(item_empty + slot, (uint32_t)(k / kItemSlots - 1) & 1u, ctl, 0x104)) {
-                        ok = false;
-                        break;
-                    }
-                    item_ring[slot] = idx;
-                    mbar_arrive(item_full + slot);
+                const int slot = k % kItemSlots;
+                if (k >= kItemSlots &&
+                    !wait_phase(item_empty + slot, (uint32_t)(k / kItemSlots - 1) & 1u, ctl, 0x104)) {
+                    ok = false;
+                    break;
                 }
+                Item it{};
+                int ntot = 0;
+                if (idx >= 0) {
+                    it = decode_item(p.g, idx);
+                    ntot = item_tiles(p, it);
+                }
+                ItemSlot &pub = item_ring[slot];
+                pub.has = idx >= 0 ? 1 : 0;
+                pub.ntot = ntot;
+                pub.it = it;
+                mbar_arrive(item_full + slot);
                 if (idx < 0)
                     break;
-                const Item it = decode_item(p.g, idx);
-                const int ntot = item_tiles(p, it);
                 if (ntot == 0)
                     continue;
                 const int ntile = it.t[1].valid ? 2 : 1;
@@ -503,14 +517,13 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             int od[2] = {0, 0};         // O_t finalisations so far, per tile
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const long long idx = take_item(k, ok, 0x206, lane);
-                if (idx < 0)
+                ItemSlot cur;
+                if (!take_item(k, ok, 0x206, lane, cur))
                     break;
-                const Item it = decode_item(p.g, idx);
-                const int ntot = item_tiles(p, it);
+                const int ntot = cur.ntot;
                 if (ntot == 0)
                     continue;
-                const int ntile = it.t[1].valid ? 2 : 1;
+                const int ntile = cur.it.t[1].valid ? 2 : 1;
                 ok = wait_phase(q_full, nq0 & 1, ctl, 0x201);
                 ++nq0;
                 tc_fence_after();
@@ -616,55 +629,85 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
         int sp = 0;  // S_t / P_t phases of this tile so far
         int od = 0;  // O_t finalisations of this tile so far
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const long long idx = take_item(k, ok, 0x303, lane);
-            if (idx < 0)
-                break;
-            const Item it = decode_item(p.g, idx);
-            const int ntot = item_tiles(p, it);
-            const int ntile = it.t[1].valid ? 2 : 1;
-            if (t >= ntile) {
-                g += ntot;
-                continue;
-            }
-            const Tile &T = it.t[t];
+        // Row set-up of this thread's row in a work item (its tile t).
+        struct Rows {
+            int ntot, ntile;
+            float *orow;     // O row (nullptr: padding row, or skipped by the checked build)
+            float *lrow;     // LSE element
+            int causal_lim;  // last allowed key of the row (inclusive) under the causal mask
+        };
+        auto setup_rows = [&](const ItemSlot &c) -> Rows {
+            Rows w;
+            w.ntot = c.ntot;
+            w.ntile = c.it.t[1].valid ? 2 : 1;
+            w.orow = nullptr;
+            w.lrow = nullptr;
+            w.causal_lim = 0x7fffffff;
+            if (t >= w.ntile)
+                return w;
+            const Tile T = t == 0 ? c.it.t[0] : c.it.t[1];
             const int head = T.h0 + r / p.g.Mq;
             const int qi = T.q0 + r % p.g.Mq;
-            const bool row_valid = (r % p.g.Mq) < T.nq;
-            float *orow = nullptr;
-            float *lrow = nullptr;
-            if (row_valid) {
-                long long row = ((long long)it.b * p.g.Hq + head) * p.g.Sq + qi;
+            if ((r % p.g.Mq) < T.nq) {
+                long long row = ((long long)c.it.b * p.g.Hq + head) * p.g.Sq + qi;
                 long long so = 0, sl = 0;
                 if (p.g.partial != kFused) {
-                    const int slot = out_slot(p, it);
+                    const int slot = out_slot(p, c.it);
                     so = slot * p.slot_o;
                     sl = slot * p.slot_lse;
                 }
-                orow = p.out + so + row * D;
-                lrow = p.lse + sl + row;
+                w.orow = p.out + so + row * D;
+                w.lrow = p.lse + sl + row;
                 if (kChecked) {
                     // element offsets (O may hold bf16 elements: same offsets)
                     const long long oo = so + row * D, lo_ = sl + row;
                     if (oo < 0 || oo + D > p.out_elems || lo_ < 0 || lo_ >= p.lse_elems) {
                         record_bounds(0x503);
-                        orow = nullptr;
-                        lrow = nullptr;
+                        w.orow = nullptr;
+                        w.lrow = nullptr;
                     }
                 }
             }
-            if (ntot == 0) {
-                // no allowed key for any row of this item in this shard
-                if (orow) {
-                    float4 *dst = reinterpret_cast<float4 *>(orow);
-                    for (int c = 0; c < D / 4; ++c)
-                        dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    *lrow = -INFINITY;
-                }
+            if (p.g.causal)
+                w.causal_lim = qi + (p.g.Skv - p.g.Sq);
+            return w;
+        };
+        // The next item is taken and set up, and this item's LSE stored, while
+        // the tensor cores finish the item's last P.V: the epilogue then runs
+        // straight into the next item's first S.
+        ItemSlot cur;
+        bool have = take_item(0, ok, 0x303, lane, cur);
+        Rows rw = have ? setup_rows(cur) : Rows{};
+        for (int k = 0; have && ok; ++k) {
+            // the fields the step loop reads: the rest of cur is not kept live
+            // across the tiles
+            Item it{};
+            it.rank = cur.it.rank;
+            it.shard = cur.it.shard;
+            it.kv_end = cur.it.kv_end;
+            const int ntot = rw.ntot;
+            const int ntile = rw.ntile;
+            if (t >= ntile) {
+                g += ntot;
+                have = take_item(k + 1, ok, 0x303, lane, cur);
+                if (have)
+                    rw = setup_rows(cur);
                 continue;
             }
-            // last allowed key of this row (inclusive) under the causal mask
-            const int causal_lim = p.g.causal ? qi + (p.g.Skv - p.g.Sq) : 0x7fffffff;
+            if (ntot == 0) {
+                // no allowed key for any row of this item in this shard
+                if (rw.orow) {
+                    float4 *dst = reinterpret_cast<float4 *>(rw.orow);
+                    for (int c = 0; c < D / 4; ++c)
+                        dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *rw.lrow = -INFINITY;
+                }
+                have = take_item(k + 1, ok, 0x303, lane, cur);
+                if (have)
+                    rw = setup_rows(cur);
+                continue;
+            }
+            const int causal_lim = rw.causal_lim;
             const bool forwards = (t == ntile - 1) && r == 0;  // reports iteration done
             float m = -INFINITY;  // running max (log2 domain), possibly stale by < 2^8
             float l = 0.f;        // running sum of 2^(y - m)
@@ -800,6 +843,14 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             g += ntot;
             if (!ok)
                 break;
+            if (rw.lrow)
+                *rw.lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            float *const orow = rw.orow;
+            have = take_item(k + 1, ok, 0x303, lane, cur);
+            if (!ok)
+                break;
+            if (have)
+                rw = setup_rows(cur);
             // ------------------------------------------------- epilogue
             bool got = wait_phase(o_full + t, od & 1, ctl, 0x302);
             ok = __all_sync(0xffffffffu, got);
@@ -897,8 +948,6 @@ attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(o_free + t);
-            if (lrow)
-                *lrow = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
         // the O tensor stores this warp issued complete before the CTA leaves
         if (lane == 0)
