@@ -418,18 +418,21 @@ int mercury_plan_shift(int R, int shift, int *order)
 int mercury_attn_sharded(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                          int d, int R, int shift, int causal, float *out, float *lse, void *stream)
 {
+    CallRange range(__func__);
     return attn_common(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, out, lse, stream, 0);
 }
 
 int mercury_attn_partial(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                          int d, int R, int shift, int causal, float *o_part, float *lse_part, void *stream)
 {
+    CallRange range(__func__);
     return attn_common(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, o_part, lse_part, stream, 1);
 }
 
 int mercury_lse_merge(const float *o_part, const float *lse_part, int n_parts, long long rows, int d,
                       float *out, float *lse, void *stream)
 {
+    CallRange range(__func__);
     if (!o_part || !lse_part || !out || !lse)
         return fail(MERCURY_EINVAL, "null pointer argument");
     if (n_parts < 1 || n_parts > 4096)
@@ -454,6 +457,7 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
                                int Skv, int d, int R, int shift, int causal, int n_runs, float *out,
                                float *lse, void *stream)
 {
+    CallRange range(__func__);
     cudaStream_t s = (cudaStream_t)stream;
     int rc = attn_split_noalloc(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_runs, out, lse,
                                 wait_budget_ns(), fault_mode(), s, g_msg, sizeof g_msg);
@@ -463,12 +467,14 @@ int mercury_attn_split_noalloc(const void *q, const void *k, const void *v, int 
 int mercury_attn_sharded_bf16(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq,
                               int Skv, int d, int R, int shift, int causal, void *out, float *lse, void *stream)
 {
+    CallRange range(__func__);
     return attn_common(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, (float *)out, lse, stream, 0, 1);
 }
 
 int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
                         int d, int n_splits, int causal, float *out, float *lse, void *stream)
 {
+    CallRange range(__func__);
     if (n_splits < 0 || n_splits > kMaxR)
         return fail(MERCURY_EINVAL, "n_splits must be in [0, %d] (got %d)", kMaxR, n_splits);
     if (n_splits > 0 && Skv % n_splits != 0)
@@ -525,6 +531,7 @@ int mercury_attn_run_schedule(const void *q, const void *k, const void *v, int B
                               int Skv, int d, int causal, const mercury_schedule *plan, float *out, float *lse,
                               void *stream)
 {
+    CallRange range(__func__);
     if (!plan)
         return fail(MERCURY_EINVAL, "plan is NULL");
     const int R = plan->R, Rq = plan->Rq, runs = plan->n_runs;
@@ -576,6 +583,7 @@ int mercury_attn_run_schedule(const void *q, const void *k, const void *v, int B
 int mercury_gemm_shifted(const void *a, const void *b, int M, int N, int K, int R, int shift, float *c,
                          void *stream)
 {
+    CallRange range(__func__);
     if (!a || !b || !c)
         return fail(MERCURY_EINVAL, "null pointer argument");
     if (M < 1 || N < 1 || K < 1)

@@ -1,11 +1,23 @@
 // internal.h -- declarations shared by the C-ABI layer and the kernel files.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 
 #include "../../include/mercury_attn.h"
 
 namespace mercury {
+
+// An NVTX range around one C call, named after it, so that a profiler can
+// pick the call's launches out of an application (for example
+// `ncu --nvtx --nvtx-include "mercury_attn_sharded/"`).  Without an attached
+// tool a range costs one well-predicted branch.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
 
 // One attention call, validated by the C-ABI layer.
 struct AttnCall {

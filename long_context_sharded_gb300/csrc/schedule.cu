@@ -509,6 +509,7 @@ int mercury_plan_schedules(int B, int Hq, int Hkv, int Sq, int Skv, int d, int c
 
 int mercury_measure_cost_profile(mercury_cost_profile *prof, void *stream)
 {
+    CallRange range(__func__);
     if (!prof)
         return set_error(MERCURY_EINVAL, "prof is NULL");
     int n = 0;
@@ -595,6 +596,7 @@ int mercury_tune_schedule(const void *q, const void *k, const void *v, int B, in
                           int d, int R, int shift, int causal, long long budget_bytes, int top_k, float *out,
                           float *lse, void *stream, mercury_schedule *best, int *cache_hit)
 {
+    CallRange range(__func__);
     if (top_k < 1 || top_k > 16)
         return set_error(MERCURY_EINVAL, "top_k must be in [1, 16] (got %d)", top_k);
     if (!q || !k || !v || !out || !lse)
