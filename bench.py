@@ -303,16 +303,20 @@ def measure_config(m, name, dev, stream, peaks, n_sms, reps):
     burst = peaks["bf16_tflops"]
     res = {"mode": "fused" if w["mode"] == "fused" else "partial+merge", "reps": reps, "flop": flops}
     if w["mode"] == "fused":
+        tw0 = time.time()
         ms = statistics.median(time_calls(
             lambda: m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream), stream, reps))
+        res["window"] = (tw0, time.time())
         tf = flops / (ms / 1e3) / 1e12
         res.update({"ms": round(ms, 4), "tflops": round(tf, 2), "frac": round(tf / burst, 4),
                     "launches_per_call": launches_per_call(m, w, n_sms)})
     else:
         op = torch.empty((R, B, Hq, Sq, d), dtype=torch.float32, device=dev)
         lp = torch.empty((R, B, Hq, Sq), dtype=torch.float32, device=dev)
+        tw0 = time.time()
         tp = statistics.median(time_calls(
             lambda: m.mercury_attn_partial(qd, kd, vd, R, w["shift"], w["causal"], op, lp, stream), stream, reps))
+        res["window"] = (tw0, time.time())
         tm = statistics.median(time_calls(lambda: m.mercury_lse_merge(op, lp, out, lse, stream), stream, reps))
         ts = statistics.median(time_calls(
             lambda: m.mercury_attn_sharded(qd, kd, vd, R, w["shift"], w["causal"], out, lse, stream), stream, reps))
@@ -332,6 +336,25 @@ def measure_config(m, name, dev, stream, peaks, n_sms, reps):
     del qd, kd, vd, out, lse
     torch.cuda.empty_cache()
     return res
+
+
+def attach_config_clocks(configs, rows, n_sms):
+    """Each timed workload's own median SM clock (nvidia-smi samples inside
+    its timed calls, warm-up included) and its TFLOP/s as a fraction of the
+    tensor pipe's ceiling at that clock: a burst long enough to reach the
+    power cap shows as a lower clock, not a lower fraction.  Bursts shorter
+    than the 25 ms sampling interval may carry no sample (null)."""
+    for name, cfg in configs.items():
+        if not isinstance(cfg, dict) or "window" not in cfg:
+            continue
+        t0, t1 = cfg.pop("window")
+        s = ClockSampler.summarise(rows, t0, t1) if rows else {"sm_mhz": None, "samples": 0}
+        mhz = s["sm_mhz"]
+        tf = cfg.get("attention_tflops", cfg.get("tflops"))
+        cp = clock_peak_tflops(n_sms, mhz)
+        cfg["sm_mhz"] = mhz
+        cfg["clock_samples"] = s["samples"]
+        cfg["clock_frac"] = round(tf / cp, 4) if cp and tf else None
 
 
 def run_gpu(args):
@@ -516,10 +539,13 @@ def run_gpu(args):
         headline = {"mode": "fused" if not partial else "partial+merge", "ms": round(statistics.median(per_step_ms), 4),
                     "tflops": round(achieved, 2), "frac": round(achieved / peaks["bf16_tflops"], 4),
                     "flop": flops, "source": "the headline timed region (%d steps)" % args.steps,
-                    "launches_per_call": launches_per_step}
+                    "launches_per_call": launches_per_step,
+                    "sm_mhz": clocks["sm_mhz"] if clocks else None,
+                    "clock_frac": round(achieved / cp, 4) if cp else None}
         configs = dict([(k_, v_) for k_, v_ in configs.items() if k_ in ("peak", "peak_kind")]
                        + [(n, headline if n == args.workload else configs[n]) for n in WORKLOADS])
         configs["clocks"] = clocks_cfg
+        attach_config_clocks(configs, rows, n_sms)
         torch.cuda.empty_cache()
         # the schedule planner's estimate (built-in profile) beside the measured time
         prof = m.mercury_default_cost_profile(n_sms)

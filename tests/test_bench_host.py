@@ -1,6 +1,7 @@
 """Host logic of bench.py without a GPU: max-over-ranks timing and whole-job
 throughput across two gloo ranks (the replica path of --gpus N), clock-log
-parsing, and the reference arm's rank filter."""
+parsing, per-workload clocks, and the reference arm's rank filter."""
+import json
 import os
 import socket
 
@@ -102,6 +103,32 @@ def test_clock_normalised_ceiling():
     assert bench.clock_peak_tflops(152, 2070) == pytest.approx(8192 * 152 * 2070e6 / 1e12)
     assert bench.clock_peak_tflops(152, 2070) == pytest.approx(2577.5, abs=0.1)
     assert bench.clock_peak_tflops(152, None) is None
+
+
+def test_config_clocks_from_each_window():
+    """Every timed workload gets the median SM clock of the samples inside its
+    own timed calls and its TFLOP/s over the tensor ceiling at that clock; a
+    window with no sample gets null; the window itself leaves the record."""
+    import datetime
+    t0 = datetime.datetime(2026, 12, 2, 10, 0, 0).timestamp()
+    row = lambda sec, mhz: ["2026/12/02 10:00:%06.3f" % sec, "0", "%d MHz" % mhz, "2070 MHz", "1000.0 W",
+                            "0x4", "Not Active", "Not Active", "Not Active", "Active"]
+    rows = [row(0.10, 2070), row(0.12, 2070), row(0.50, 1750), row(0.52, 1760), row(0.54, 1770)]
+    configs = {
+        "peak": 1902.6,
+        "a": {"tflops": 1800.0, "window": (t0 + 0.05, t0 + 0.2)},
+        "b": {"attention_tflops": 1700.0, "tflops": 1690.0, "window": (t0 + 0.45, t0 + 0.6)},
+        "c": {"tflops": 10.0, "window": (t0 + 0.3, t0 + 0.31)},
+        "clocks": {"sm_mhz": 2070},
+    }
+    bench.attach_config_clocks(configs, rows, 152)
+    assert configs["a"]["sm_mhz"] == 2070 and configs["a"]["clock_samples"] == 2
+    assert configs["a"]["clock_frac"] == pytest.approx(1800.0 / bench.clock_peak_tflops(152, 2070), abs=1e-4)
+    assert configs["b"]["sm_mhz"] == 1760
+    assert configs["b"]["clock_frac"] == pytest.approx(1700.0 / bench.clock_peak_tflops(152, 1760), abs=1e-4)
+    assert configs["c"]["sm_mhz"] is None and configs["c"]["clock_frac"] is None
+    assert all("window" not in v for v in configs.values() if isinstance(v, dict))
+    json.dumps(configs)
 
 
 def test_launches_per_call_follows_the_library_schedule(monkeypatch):
