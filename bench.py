@@ -249,20 +249,11 @@ def device_qkv(w, dev):
 
 def launches_per_call(m, w, n_sms: int) -> int:
     """Kernels one mercury_attn_sharded call launches: 1 for the fused
-    schedule, 2 when the library's chooser splits it (attention + merge).  The
-    chooser takes the fastest predicted run count with Rq = R whose scratch
-    fits in 4 GiB; the same planner gives the same answer here."""
-    prof = m.mercury_default_cost_profile(n_sms)
-    plans, _ = m.mercury_plan_schedules(w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], w["causal"],
-                                        w["R"], w["shift"], 0, prof, 512)
-    cap = int(os.environ.get("MERCURY_SCRATCH_MAX_BYTES", str(4 << 30)))
-    forced = int(os.environ.get("MERCURY_SPLIT_GROUPS", "0") or 0)
-    if forced >= 1:
-        return 1 if forced == 1 or w["R"] == 1 else 2
-    for p in plans:
-        if p.Rq == w["R"] and p.scratch_bytes <= cap:
-            return 1 if p.n_runs == 1 else 2
-    return 1
+    schedule, 2 when the library's chooser splits it (attention + merge),
+    as the library itself reports its choice for this shape."""
+    runs = m.mercury_choose_runs(w["B"], w["Hq"], w["Hkv"], w["Sq"], w["Skv"], w["d"], w["causal"],
+                                 w["R"], w["shift"], n_sms)
+    return 1 if runs == 1 else 2
 
 
 def clock_peak_tflops(n_sms: int, sm_mhz):

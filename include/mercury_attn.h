@@ -414,6 +414,30 @@ MERCURY_API int mercury_plan_schedules(int B, int Hq, int Hkv, int Sq, int Skv, 
                                        mercury_schedule *plans, int max_plans, int *n_plans);
 
 /*
+ * mercury_choose_runs -- the run count mercury_attn_sharded (and
+ * mercury_attn_sharded_bf16) uses for a call of this shape on a device with
+ * n_sms SMs: the n_runs that mercury_plan_schedules' estimate with the
+ * built-in profile (this R, Rq = R) predicts fastest among those whose
+ * scratch, n_runs * B*Hq*Sq*(d+1)*4 bytes, fits in scratch_cap bytes (ties:
+ * fewer runs); scratch_cap < 0 takes mercury_attn_sharded's cap (env
+ * MERCURY_SCRATCH_MAX_BYTES, default 4 GiB); env MERCURY_SPLIT_GROUPS=g
+ * forces min(g, R) as it does for the call; R == 1 gives 1.  The search is
+ * the pages' staged one -- a static memory check, then a cost estimate
+ * (Mercury-SOSP25 paper notes, 核心方法 and 设计取舍) -- kept cheap because
+ * a new shape's first call waits for it (time to first usable schedule:
+ * Silicon & Systems, "The tuning bill"): a candidate whose lower bound (its
+ * work items' summed cost spread over n_sms CTAs, its longest item, its
+ * least memory traffic, plus the merge) is no better than the best so far is
+ * not estimated further, which leaves the answer unchanged.  Pure host code,
+ * no GPU; the answer is remembered per shape.
+ * Requirements: as mercury_attn_sharded for the shape; n_sms >= 1; n_runs
+ * not NULL.  Errors: MERCURY_EINVAL.
+ */
+MERCURY_API int mercury_choose_runs(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal,
+                                    int R, int shift, int n_sms, long long scratch_cap,
+                                    int *n_runs);
+
+/*
  * mercury_attn_run_schedule -- attention by a given schedule (one of
  * mercury_plan_schedules' candidates, or any valid tuple).  Arguments and
  * layouts as mercury_attn_sharded; the schedule's R, Rq, n_runs and shift

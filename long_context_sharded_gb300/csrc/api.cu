@@ -92,11 +92,9 @@ int check_shift(int R, int shift)
     return MERCURY_OK;
 }
 
-int check_attn_args(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
-                    int d, int R, int shift, int causal, const float *out, const float *lse, int partial)
+// The shape of an attention call (no pointers).
+int check_attn_shape(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int shift, int causal, int partial)
 {
-    if (!q || !k || !v || !out || !lse)
-        return fail(MERCURY_EINVAL, "null pointer argument");
     if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1)
         return fail(MERCURY_EINVAL, "B, Hq, Hkv, Sq, Skv must be >= 1");
     if (Hq % Hkv != 0)
@@ -117,6 +115,17 @@ int check_attn_args(const void *q, const void *k, const void *v, int B, int Hq, 
         return fail(MERCURY_EINVAL, "tensor sizes overflow");
     if ((long long)B * Hq > INT_MAX || (long long)B * Hkv > INT_MAX)
         return fail(MERCURY_EINVAL, "B*H exceeds 2^31");
+    return MERCURY_OK;
+}
+
+int check_attn_args(const void *q, const void *k, const void *v, int B, int Hq, int Hkv, int Sq, int Skv,
+                    int d, int R, int shift, int causal, const float *out, const float *lse, int partial)
+{
+    if (!q || !k || !v || !out || !lse)
+        return fail(MERCURY_EINVAL, "null pointer argument");
+    int rc = check_attn_shape(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, partial);
+    if (rc)
+        return rc;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
         return fail(MERCURY_EALIGN, "q, k, v and the O output must be 16-byte aligned");
     if (!aligned(lse, 4))
@@ -203,14 +212,17 @@ long long env_ll(const char *name, long long dflt)
 // The run count is the one schedule.cu's cost model predicts fastest among
 // those whose scratch fits in MERCURY_SCRATCH_MAX_BYTES (default 4 GiB).
 // Returns the number of runs (1 = fused).  MERCURY_SPLIT_GROUPS forces it.
-int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int shift, int causal, int sms)
+// cap < 0: the scratch cap of mercury_attn_sharded (env or 4 GiB).
+int choose_groups(int B, int Hq, int Hkv, int Sq, int Skv, int d, int R, int shift, int causal, int sms,
+                  long long cap = -1)
 {
     long long forced = env_ll("MERCURY_SPLIT_GROUPS", 0);
     if (forced >= 1)
         return (int)(forced < R ? forced : R);
     if (R == 1 || sms < 1)
         return 1;
-    const long long cap = env_ll("MERCURY_SCRATCH_MAX_BYTES", 4LL << 30);
+    if (cap < 0)
+        cap = env_ll("MERCURY_SCRATCH_MAX_BYTES", 4LL << 30);
     return best_run_count(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, sms, cap);
 }
 
@@ -412,6 +424,20 @@ int mercury_plan_shift(int R, int shift, int *order)
         return rc;
     if (plan_shift(R, shift, order))
         return fail(MERCURY_EINVAL, "invalid (R, shift)");
+    return ok();
+}
+
+int mercury_choose_runs(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int R, int shift, int n_sms,
+                        long long scratch_cap, int *n_runs)
+{
+    if (!n_runs)
+        return fail(MERCURY_EINVAL, "n_runs is NULL");
+    int rc = check_attn_shape(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, 0);
+    if (rc)
+        return rc;
+    if (n_sms < 1)
+        return fail(MERCURY_EINVAL, "n_sms must be >= 1 (got %d)", n_sms);
+    *n_runs = choose_groups(B, Hq, Hkv, Sq, Skv, d, R, shift, causal, n_sms, scratch_cap);
     return ok();
 }
 

@@ -84,6 +84,77 @@ double traffic_floor_us(const Geom &g, const mercury_cost_profile &p)
     return (in + outb) / (p.hbm_gbs * 1e3);
 }
 
+// The costs of a launch's items in launch order, each computed once: an
+// item's cost depends on its rows, rank, run and head pair but not on its
+// batch or KV head, so fused items of one (batch, KV head) -- consecutive --
+// repeat their costs with period NHP * NRT * Rq, and the other modes' items
+// come in runs of NHP * Hkv * B that differ only by head pair.
+class ItemCosts {
+  public:
+    ItemCosts(const Geom &g, const int *order, const mercury_cost_profile &p)
+        : g_(g), order_(order), p_(p), fused_(g.partial == kFused),
+          period_(fused_ ? (long long)g.NHP * g.NRT * g.Rq : 0),
+          inner_((long long)g.NHP * g.Hkv * g.B), nhp_(std::min<int>(g.NHP, kMaxR))
+    {
+        if (fused_) {
+            cost_.resize((size_t)std::min(period_, g.n_items));
+            for (long long j = 0; j < (long long)cost_.size(); ++j)
+                cost_[(size_t)j] = item_cost(g, decode_item(g, j), order, p);
+        }
+    }
+    // cost of item i, called for i = 0, 1, 2, ... in turn
+    double next(long long i)
+    {
+        double c;
+        if (fused_) {
+            c = cost_[(size_t)j_];
+            if (++j_ == period_)
+                j_ = 0;
+            return c;
+        }
+        if (in_run_ < nhp_)
+            run_cost_[in_run_] = item_cost(g_, decode_item(g_, i), order_, p_);
+        c = hp_ < nhp_ ? run_cost_[hp_] : item_cost(g_, decode_item(g_, i), order_, p_);
+        if (++hp_ == g_.NHP)
+            hp_ = 0;
+        if (++in_run_ == inner_) {
+            in_run_ = 0;
+            hp_ = 0;
+        }
+        return c;
+    }
+
+  private:
+    const Geom &g_;
+    const int *order_;
+    const mercury_cost_profile &p_;
+    bool fused_;
+    long long period_, inner_;
+    int nhp_;
+    std::vector<double> cost_;
+    double run_cost_[kMaxR];
+    long long j_ = 0, in_run_ = 0;  // i % period, i % inner
+    int hp_ = 0;                    // in_run % NHP
+};
+
+// A lower bound on launch_estimate: no launch ends before the average CTA's
+// share of the item costs, its longest item or its least HBM traffic.
+double launch_lower_bound(const Geom &g, const int *order, const mercury_cost_profile &p)
+{
+    const long long n = g.n_items;
+    if (n <= 0)
+        return p.launch_us;
+    const long long grid = std::min<long long>(n, p.n_sms);
+    ItemCosts ic(g, order, p);
+    double sum = 0.0, longest = 0.0;
+    for (long long i = 0; i < n; ++i) {
+        const double c = ic.next(i);
+        sum += c;
+        longest = std::max(longest, c);
+    }
+    return p.launch_us + std::max(std::max(sum / (double)grid, longest), traffic_floor_us(g, p));
+}
+
 // Device time of one launch of geometry g on min(n_items, n_sms) persistent
 // CTAs: the launch lasts as long as its busiest CTA, plus the launch cost.
 // Items go round robin in launch order -- except in causal launches with
@@ -97,17 +168,37 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
         return p.launch_us;
     const long long grid = std::min<long long>(n, p.n_sms);
     if (g.causal && n > grid) {
-        using Slot = std::pair<double, long long>;  // (busy until, CTA)
-        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+        ItemCosts ic(g, order, p);
+        // Min-heap of (busy until, CTA): the next item goes to its root, whose
+        // time then only grows, so one sift-down restores the heap.  All CTAs
+        // start free at 0 in index order, which is already a heap.
+        using Slot = std::pair<double, long long>;
+        std::vector<Slot> heap((size_t)grid);
         for (long long c = 0; c < grid; ++c)
-            free_at.push(Slot(0.0, c));
+            heap[(size_t)c] = Slot(0.0, c);
         double last = 0.0;
         for (long long i = 0; i < n; ++i) {
-            Slot s = free_at.top();
-            free_at.pop();
-            s.first += item_cost(g, decode_item(g, i), order, p);
+            const double c = ic.next(i);
+            Slot s = heap[0];
+            s.first += c;
             last = std::max(last, s.first);
-            free_at.push(s);
+            size_t k = 0;
+            for (;;) {
+                const size_t l = 2 * k + 1, r = l + 1;
+                size_t m = k;
+                const Slot *best = &s;
+                if (l < heap.size() && heap[l] < *best) {
+                    m = l;
+                    best = &heap[l];
+                }
+                if (r < heap.size() && heap[r] < *best)
+                    m = r;
+                if (m == k)
+                    break;
+                heap[k] = heap[m];
+                k = m;
+            }
+            heap[k] = s;
         }
         return p.launch_us + std::max(last, traffic_floor_us(g, p));
     }
@@ -181,7 +272,7 @@ int check_profile(const mercury_cost_profile *p)
 // Estimate of one schedule, or a negative number if the shape does not
 // admit it.
 double estimate(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int R, int Rq, int runs, int shift,
-                const mercury_cost_profile &p, long long *items)
+                const mercury_cost_profile &p, long long *items, bool lower_bound = false)
 {
     int mode, groups;
     mode_of(R, runs, mode, groups);
@@ -192,7 +283,7 @@ double estimate(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, int 
     if (plan_shift(R, shift, order))
         return -1.0;
     *items = g.n_items;
-    double t = launch_estimate(g, order, p);
+    double t = lower_bound ? launch_lower_bound(g, order, p) : launch_estimate(g, order, p);
     if (g.partial != kFused) {
         const double rows = (double)B * Hq * Sq;
         const double bytes = (g.n_groups + 1.0) * rows * (d + 1) * 4.0;
@@ -439,6 +530,13 @@ int best_run_count(int B, int Hq, int Hkv, int Sq, int Skv, int d, int causal, i
         if (runs > 1 && scratch_bytes_of(B, Hq, Sq, d, runs >= R ? R : runs) > scratch_cap)
             break;
         long long items = 0;
+        // A candidate whose lower bound is no better than the best so far
+        // cannot win: skip its full estimate (the simulation of a causal
+        // launch's dynamic scheduling costs ~70 ns per work item).  The margin
+        // covers the different summation order of the bound.
+        if (best_t >= 0 &&
+            estimate(B, Hq, Hkv, Sq, Skv, d, causal, R, R, runs, shift, p, &items, true) * (1.0 - 1e-9) >= best_t)
+            continue;
         const double t = estimate(B, Hq, Hkv, Sq, Skv, d, causal, R, R, runs, shift, p, &items);
         if (t >= 0 && (best_t < 0 || t < best_t)) {
             best_t = t;

@@ -12,6 +12,7 @@ The functions keep the C names:
   mercury_lse_merge(o_part, lse_part, out=None, lse=None, stream=None)
   mercury_sync_status(stream=None)
   mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, budget_bytes, profile)
+  mercury_choose_runs(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, n_sms, scratch_cap=-1) -> int
   mercury_attn_run_schedule(q, k, v, causal, plan, out=None, lse=None, stream=None)
   mercury_tune_schedule(q, k, v, R, shift, causal, budget_bytes, top_k, ...)
 Tensors: q [B,Hq,Sq,d], k/v [B,Hkv,Skv,d] bf16 CUDA tensors, contiguous.
@@ -48,7 +49,7 @@ EXPORTED = ("mercury_plan_shift", "mercury_attn_sharded", "mercury_attn_partial"
             "mercury_gemm_shifted", "mercury_attn_decode", "mercury_attn_sharded_bf16",
             "mercury_default_cost_profile", "mercury_measure_cost_profile",
             "mercury_plan_schedules", "mercury_attn_run_schedule", "mercury_tune_schedule",
-            "mercury_tune_cache_clear")
+            "mercury_tune_cache_clear", "mercury_choose_runs")
 
 
 class CostProfile(ctypes.Structure):
@@ -116,6 +117,7 @@ def _load() -> ctypes.CDLL:
     lib.mercury_tune_schedule.argtypes = [p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, i32, i64,
                                           i32, p, p, p, p, p]
     lib.mercury_tune_cache_clear.argtypes = []
+    lib.mercury_choose_runs.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, i64, p]
     for name in EXPORTED:
         if name not in ("mercury_last_error", "mercury_tune_cache_clear"):
             getattr(lib, name).restype = i32
@@ -368,6 +370,14 @@ def mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, budget_byte
                                       int(budget_bytes), ctypes.byref(profile), plans,
                                       int(max_plans), ctypes.byref(n)))
     return [plans[i] for i in range(min(n.value, int(max_plans)))], n.value
+
+
+def mercury_choose_runs(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, n_sms, scratch_cap=-1) -> int:
+    """The run count mercury_attn_sharded uses for this shape on n_sms SMs (host only)."""
+    n = ctypes.c_int(0)
+    _check(lib.mercury_choose_runs(B, Hq, Hkv, Sq, Skv, d, int(bool(causal)), R, shift, int(n_sms),
+                                   int(scratch_cap), ctypes.byref(n)))
+    return n.value
 
 
 def _schedule(plan):

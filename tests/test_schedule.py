@@ -208,6 +208,56 @@ def test_closed_forms(m):
     del prof
 
 
+CHOOSE_SHAPES = [
+    # B, Hq, Hkv, Sq, Skv, d, causal, R, shift
+    (1, 32, 8, 32768, 32768, 128, True, 8, 1),
+    (1, 64, 8, 131072, 131072, 128, True, 8, 4),
+    (16, 32, 32, 4096, 4096, 128, False, 8, 1),
+    (1, 8, 1, 2048, 2097152, 128, False, 64, 1),
+    (1, 4, 4, 512, 512, 64, False, 4, 1),
+    (1, 8, 1, 64, 131072, 128, True, 16, 1),
+    (2, 24, 8, 6144, 6144, 64, True, 8, 2),
+    (1, 40, 8, 3072, 4096, 128, True, 4, 1),
+    (3, 12, 4, 1536, 1536, 128, True, 16, 4),
+    (1, 16, 2, 256, 65536, 128, False, 32, 0),
+    (4, 8, 8, 1024, 1024, 64, True, 8, 1),
+]
+
+
+@pytest.mark.parametrize("cap", [-1, 0, 200 << 20])
+@pytest.mark.parametrize("shape", CHOOSE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_choose_runs_is_the_planner_argmin(m, shape, cap, monkeypatch):
+    """The run count mercury_attn_sharded uses is the planner's fastest Rq = R
+    candidate whose scratch fits the cap (ties: fewer runs), although the
+    chooser skips candidates by their lower bound instead of estimating all."""
+    monkeypatch.delenv("MERCURY_SPLIT_GROUPS", raising=False)
+    monkeypatch.delenv("MERCURY_SCRATCH_MAX_BYTES", raising=False)
+    B, Hq, Hkv, Sq, Skv, d, causal, R, shift = shape
+    prof = m.mercury_default_cost_profile(152)
+    plans, _ = m.mercury_plan_schedules(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, 0, prof, 512)
+    limit = (4 << 30) if cap < 0 else cap
+    fits = [p for p in plans if p.Rq == R and (p.n_runs == 1 or p.scratch_bytes <= limit)]
+    best = min(fits, key=lambda p: (p.predicted_us, p.n_runs))
+    assert m.mercury_choose_runs(B, Hq, Hkv, Sq, Skv, d, causal, R, shift, 152, cap) == best.n_runs
+
+
+def test_choose_runs_forced_and_rejects(m, monkeypatch):
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "3")
+    assert m.mercury_choose_runs(1, 8, 1, 2048, 2097152, 128, False, 64, 1, 152) == 3
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "100")
+    assert m.mercury_choose_runs(1, 8, 1, 2048, 2097152, 128, False, 64, 1, 152) == 64
+    monkeypatch.delenv("MERCURY_SPLIT_GROUPS")
+    assert m.mercury_choose_runs(1, 8, 8, 256, 256, 128, False, 1, 1, 152) == 1
+    for args in [(1, 8, 3, 256, 256, 128, False, 8, 1, 152), (1, 8, 8, 256, 256, 96, False, 8, 1, 152),
+                 (1, 8, 8, 256, 250, 128, False, 8, 1, 152), (1, 8, 8, 256, 256, 128, False, 8, 1, 0),
+                 (1, 8, 8, 512, 256, 128, True, 8, 1, 152)]:
+        with pytest.raises(m.MercuryError) as e:
+            m.mercury_choose_runs(*args)
+        assert e.value.status == m.MERCURY_EINVAL
+    n = ctypes.c_int(0)
+    assert m.lib.mercury_choose_runs(1, 8, 8, 256, 256, 128, 0, 8, 1, 152, -1, None) == m.MERCURY_EINVAL
+
+
 def test_choose_r(m):
     prof = m.mercury_default_cost_profile(152)
     plans, n = m.mercury_plan_schedules(1, 8, 2, 768, 1536, 128, True, 0, 1, 0, prof)
