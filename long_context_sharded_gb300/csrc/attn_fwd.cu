@@ -10,7 +10,8 @@
 //
 // One persistent CTA per SM takes work items in turn (a work item: up to two
 // 128-row query tiles sharing a KV head, one (batch, KV head) at a time):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles into two
+//   warp 0      TMA producer: decodes and publishes the CTA's work items,
+//               loads Q tiles once, then K and V tiles into two
 //               shared-memory rings, in the shifted shard order
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane
 //               issues): S_t = Q_t K^T and O_t += P_t V on the tensor cores
@@ -233,9 +234,12 @@ __device__ __forceinline__ int item_tiles(const AttnParams &p, const Item &it)
 }
 
 // Persistent: each CTA (one per SM) takes work items blockIdx.x,
-// blockIdx.x + gridDim.x, ...  (heaviest first for causal calls).  Barrier
-// phases run on across items; the MMA issuer starts the next item's Q K^T
-// while the softmax warps still write out the previous item's O.
+// blockIdx.x + gridDim.x, ...  (heaviest first for causal calls, which claim
+// their items dynamically); its TMA producer decodes each item once and
+// publishes it to the other roles.  Barrier phases run on across items; the
+// MMA issuer starts the next item's Q K^T while the softmax warps still write
+// out the previous item's O, and the softmax warps set up the next item
+// before that epilogue.
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
