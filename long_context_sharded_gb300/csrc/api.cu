@@ -307,9 +307,6 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     int rc = check_attn_args(q, k, v, B, Hq, Hkv, Sq, Skv, d, R, shift, causal, out, lse, partial);
     if (rc)
         return rc;
-    int order[kMaxR * kMaxR];
-    if (plan_shift(R, shift, order))
-        return fail(MERCURY_EINVAL, "invalid (R, shift)");
     cudaStream_t s = (cudaStream_t)stream;
     int groups = 1;
     if (!partial) {
@@ -337,7 +334,7 @@ int attn_common(const void *q, const void *k, const void *v, int B, int Hq, int 
     c.mode = (partial || groups >= R) ? kPerStep : (groups > 1 ? kGrouped : kFused);
     c.n_groups = (partial || groups >= R) ? R : groups;
     c.Rq = R;
-    c.order = order;
+    c.shift = shift;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
     if (partial) {
@@ -529,8 +526,6 @@ int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int 
                 break;
         }
     }
-    int order[kMaxR * kMaxR];
-    plan_shift(splits, 1, order);  // rank 0 reads shard j at step j
     AttnCall c;
     c.q = q;
     c.k = k;
@@ -546,7 +541,7 @@ int mercury_attn_decode(const void *q, const void *k, const void *v, int B, int 
     c.causal = causal ? 1 : 0;
     c.mode = splits == 1 ? kFused : kPerStep;
     c.n_groups = splits;
-    c.order = order;
+    c.shift = 1;  // rank 0 reads shard j at step j
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
     rc = run_to_output(c, out, lse, s);
@@ -580,8 +575,6 @@ int mercury_attn_run_schedule(const void *q, const void *k, const void *v, int B
     if (!mul_ok(n, runs) || !mul_ok(n, B) || !mul_ok(n, Hq) || !mul_ok(n, Sq) || !mul_ok(n, d + 1) ||
         !mul_ok(n, 4))
         return fail(MERCURY_EINVAL, "scratch size overflows");
-    int order[kMaxR * kMaxR];
-    plan_shift(R, plan->shift, order);
     AttnCall c;
     c.q = q;
     c.k = k;
@@ -598,7 +591,7 @@ int mercury_attn_run_schedule(const void *q, const void *k, const void *v, int B
     // as mercury_attn_sharded: one run per step takes the shard-major order
     c.mode = runs == 1 ? kFused : (runs >= R ? kPerStep : kGrouped);
     c.n_groups = runs >= R ? R : runs;
-    c.order = order;
+    c.shift = plan->shift;
     c.wait_ns = wait_budget_ns();
     c.fault = fault_mode();
     cudaStream_t s = (cudaStream_t)stream;

@@ -67,6 +67,12 @@ __device__ unsigned int g_err_site = 0;
 constexpr int kItemCounterSlots = 4096;
 __device__ unsigned int g_item_counters[kItemCounterSlots];
 
+// Kernel parameters.  The shift table's capacity TC (R <= TC) is a template
+// parameter: the whole block travels with every launch, and a 128 x 128 table
+// (16 KB) costs the host ~5 us per launch, so calls with R <= 32 take a 1 KB
+// table.  (Computing the shard in the kernel instead was measured slower on
+// short work items.)
+template <int TC>
 struct AttnParams {
     Geom g;
     float scale_log2;        // log2(e) / sqrt(d)
@@ -88,8 +94,9 @@ struct AttnParams {
     unsigned int *item_counter;
     // fused, grouped: tab[i*R + j] = shard of rank i at step j;
     // per step: tab[i*R + s] = step (slot) at which rank i reads shard s.
-    unsigned char tab[kMaxR * kMaxR];
+    unsigned char tab[TC * TC];
 };
+constexpr int kSmallTab = 32;  // table capacity of calls with R <= 32
 
 namespace {
 
@@ -171,7 +178,8 @@ __device__ __forceinline__ bool drain_phase(uint64_t *bar, uint32_t parity, Ctl 
 
 // Shard visited at step `step` of the item's sequence (fused: the rank's R
 // steps; per step: the item's shard; grouped: the item's run of steps).
-__device__ __forceinline__ int shard_at(const AttnParams &p, const Item &it, int step)
+template <int TC>
+__device__ __forceinline__ int shard_at(const AttnParams<TC> &p, const Item &it, int step)
 {
     if (p.g.partial == kPerStep)
         return it.shard;
@@ -180,7 +188,8 @@ __device__ __forceinline__ int shard_at(const AttnParams &p, const Item &it, int
 }
 
 // Output slot of a non-fused item: the step (per step) or the run (grouped).
-__device__ __forceinline__ int out_slot(const AttnParams &p, const Item &it)
+template <int TC>
+__device__ __forceinline__ int out_slot(const AttnParams<TC> &p, const Item &it)
 {
     return p.g.partial == kPerStep ? (int)p.tab[it.rank * p.g.R + it.shard] : it.shard;
 }
@@ -215,14 +224,16 @@ constexpr uint32_t kRegsSoftmax = 200;
 constexpr int kMinLaunchRegs = (int)((kRegsProducer + 2 * kRegsSoftmax) * 128 + kThreads - 1) / kThreads;
 
 // Key range [lo, hi) of step st of an item; returns its number of KV tiles.
-__device__ __forceinline__ int step_range(const AttnParams &p, const Item &it, int st, int &lo, int &hi)
+template <int TC>
+__device__ __forceinline__ int step_range(const AttnParams<TC> &p, const Item &it, int st, int &lo, int &hi)
 {
     shard_range(p.g, it, shard_at(p, it, st), lo, hi);
     return n_kv_tiles(lo, hi);
 }
 
 // KV tiles of the item's whole shifted sequence.
-__device__ __forceinline__ int item_tiles(const AttnParams &p, const Item &it)
+template <int TC>
+__device__ __forceinline__ int item_tiles(const AttnParams<TC> &p, const Item &it)
 {
     int n = 0;
     const int ns = item_steps(p.g, it);
@@ -240,9 +251,9 @@ __device__ __forceinline__ int item_tiles(const AttnParams &p, const Item &it)
 // MMA issuer starts the next item's Q K^T while the softmax warps still write
 // out the previous item's O, and the softmax warps set up the next item
 // before that epilogue.
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, int TC>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_fwd_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmQ,
+attn_fwd_kernel(const __grid_constant__ AttnParams<TC> p, const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const __grid_constant__ CUtensorMap tmO)
 {
@@ -1063,12 +1074,12 @@ int claim_item_counter(cudaStream_t stream, unsigned int **out, char *msg, size_
     return MERCURY_OK;
 }
 
-template <int D, int NK, int NV>
-int launch_impl(AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+template <int D, int NK, int NV, int TC>
+int launch_impl(AttnParams<TC> &p, const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                 const CUtensorMap &mo, cudaStream_t stream, char *msg, size_t msg_len)
 {
     using L = Smem<D, NK, NV>;
-    auto kern = attn_fwd_kernel<D, NK, NV>;
+    auto kern = attn_fwd_kernel<D, NK, NV, TC>;
     KernelInfo ki;
     int rc = prepare_kernel((const void *)kern, L::kAlloc, &ki, msg, msg_len);
     if (rc != MERCURY_OK)
@@ -1110,12 +1121,18 @@ int launch_impl(AttnParams &p, const CUtensorMap &mq, const CUtensorMap &mk, con
 
 }  // namespace
 
-int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len)
+template <int TC>
+int launch_with_table(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len)
 {
-    // The parameter block (16 KB of shift table) lives in thread-local
+    // The parameter block and the planner's table live in thread-local
     // storage: the launch path makes no heap allocation.
-    static thread_local AttnParams p;
+    static thread_local AttnParams<TC> p;
+    static thread_local int order[kMaxR * kMaxR];
     memset(&p, 0, sizeof p);
+    if (c.R < 1 || c.R > TC || plan_shift(c.R, c.shift, order)) {
+        snprintf(msg, msg_len, "invalid (R, shift) = (%d, %d)", c.R, c.shift);
+        return MERCURY_EINVAL;
+    }
     if (make_geom(p.g, c.B, c.Hq, c.Hkv, c.Sq, c.Skv, c.d, c.R, c.causal, c.mode, c.n_groups, c.Rq)) {
         snprintf(msg, msg_len, "unsupported shape");
         return MERCURY_EINVAL;
@@ -1139,7 +1156,7 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
     const int R = c.R;
     for (int i = 0; i < R; ++i)
         for (int j = 0; j < R; ++j) {
-            const int s = c.order[i * R + j];
+            const int s = order[i * R + j];
             if (c.mode == kPerStep)
                 p.tab[i * R + s] = (unsigned char)j;
             else
@@ -1160,11 +1177,17 @@ int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t m
         rc = encode_2d_f32(&mo, c.out, (uint64_t)c.d, (uint64_t)p.o_rows, 32, 32, msg, msg_len);
     if (rc == MERCURY_OK) {
         if (c.d == 128)
-            rc = launch_impl<128, 2, 2>(p, mq, mk, mv, mo, stream, msg, msg_len);
+            rc = launch_impl<128, 2, 2, TC>(p, mq, mk, mv, mo, stream, msg, msg_len);
         else
-            rc = launch_impl<64, 4, 4>(p, mq, mk, mv, mo, stream, msg, msg_len);
+            rc = launch_impl<64, 4, 4, TC>(p, mq, mk, mv, mo, stream, msg, msg_len);
     }
     return rc;
+}
+
+int launch_attention(const AttnCall &c, cudaStream_t stream, char *msg, size_t msg_len)
+{
+    return c.R <= kSmallTab ? launch_with_table<kSmallTab>(c, stream, msg, msg_len)
+                            : launch_with_table<kMaxR>(c, stream, msg, msg_len);
 }
 
 int read_and_clear_device_error(cudaStream_t stream, unsigned int *word, unsigned int *site, char *msg,

@@ -26,7 +26,7 @@ struct AttnCall {
     int mode = 0;            // kFused, kPerStep or kGrouped (work.h)
     int n_groups = 1;        // kGrouped: runs of steps per rank
     int Rq = 0;              // query blocks: R, or 1 for a decode split
-    const int *order = nullptr;  // [R*R] shift table from the planner
+    int shift = 1;           // shift order as in mercury_plan_shift (validated for R by the caller)
     float *out = nullptr, *lse = nullptr;  // fused: out/lse; otherwise [slots][B,Hq,Sq,(d)] partials
     unsigned long long wait_ns = 2000000000ull;
     int fault = 0;

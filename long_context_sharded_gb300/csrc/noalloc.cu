@@ -104,8 +104,7 @@ int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int H
         snprintf(msg, msg_len, "need 1 <= R <= %d and 1 <= n_runs <= R (R %d, n_runs %d)", kMaxR, R, n_runs);
         return MERCURY_EINVAL;
     }
-    int order[kMaxR * kMaxR];
-    if (plan_shift(R, shift, order)) {
+    if (shift < 0 || (shift >= 2 && R % shift != 0)) {
         snprintf(msg, msg_len, "invalid shift %d for R = %d", shift, R);
         return MERCURY_EINVAL;
     }
@@ -155,7 +154,7 @@ int attn_split_noalloc(const void *q, const void *k, const void *v, int B, int H
     c.mode = kGrouped;
     c.n_groups = n_runs;
     c.Rq = R;
-    c.order = order;
+    c.shift = shift;
     c.out = o_part;
     c.lse = l_part;
     c.wait_ns = wait_ns;

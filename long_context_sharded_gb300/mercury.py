@@ -142,21 +142,34 @@ def _stream_ptr(stream):
     return stream.cuda_stream
 
 
+_DTYPES = {}
+
+
+def _dtype(name):
+    """torch dtype object for "torch.bfloat16" / "torch.float32" (looked up once)."""
+    dt = _DTYPES.get(name)
+    if dt is None:
+        import torch
+        dt = _DTYPES[name] = getattr(torch, name.split(".", 1)[1])
+    return dt
+
+
 def _dev_ptr(t, dtype_name, what):
     """Device pointer of a contiguous CUDA tensor of the given dtype on the
     current device (the library runs on the current device, and a pointer
-    into another device's memory would be read there)."""
+    into another device's memory would be read there).  Small calls are
+    bound by this marshalling, so the checks use the cheapest tensor queries."""
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch tensor" % what)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % what)
-    if str(t.dtype) != dtype_name:
+    if t.dtype is not _dtype(dtype_name):
         raise TypeError("%s must be %s (got %s)" % (what, dtype_name, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % what)
     cur = torch.cuda.current_device()
-    if t.device.index != cur:
+    if t.get_device() != cur:
         raise ValueError("%s is on %s but the current device is cuda:%d" % (what, t.device, cur))
     return t.data_ptr()
 
