@@ -56,9 +56,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources, first 16 hex digits).  Reported as null once the kernel
 # has changed or when no capture of that workload exists.
 ATTN_TRAFFIC = {
-    "gqa_b1_hq32_hkv8_d128_s32k_causal_r8": {"source_sha": "71413d9e4c1b71c4", "bytes_per_launch": 897159168},
-    "gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4": {"source_sha": "71413d9e4c1b71c4",
-                                                         "bytes_per_launch": 10284272384},
+    "gqa_b1_hq32_hkv8_d128_s32k_causal_r8": {"source_sha": "50aaebb7f3354221", "bytes_per_launch": 896964864},
+    "gqa_b1_hq64_hkv8_d128_s128k_causal_r8_nested2x4": {"source_sha": "50aaebb7f3354221",
+                                                         "bytes_per_launch": 10273945856},
 }
 
 
