@@ -134,8 +134,15 @@ def _check(rc: int) -> None:
 
 
 def _stream_ptr(stream):
+    """cudaStream_t of `stream`, or of the current stream of the current
+    device.  The raw getter avoids building a torch Stream object, which costs
+    more host time than the library's whole launch path on small calls; the
+    public call is the fallback where the getter is absent."""
     if stream is None:
         import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream

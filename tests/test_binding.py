@@ -132,3 +132,19 @@ def test_structs_match_header(m):
         fields = _header_struct_fields(cname)
         assert fields, cname
         assert [(n, ctype[t]) for t, n in fields] == list(py._fields_), cname
+
+
+@pytest.mark.gpu
+def test_default_stream_pointer_is_the_current_stream(m):
+    """Calls without stream= run on the caller's current stream: the raw
+    stream getter gives the same handle as torch's public current_stream(),
+    on the default stream and inside a stream context."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    assert m._stream_ptr(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert m._stream_ptr(None) == s.cuda_stream == torch.cuda.current_stream().cuda_stream
+    assert m._stream_ptr(None) == torch.cuda.current_stream().cuda_stream
+    assert m._stream_ptr(s) == s.cuda_stream
+    assert m._stream_ptr(s.cuda_stream) == s.cuda_stream
