@@ -638,14 +638,23 @@ def run_gpu_shifted(args):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # rank 0 samples its own GPU's clocks during the timed region
+    sampler = ClockSampler(local)
+    sampling = rank == 0 and not args.no_clocks
+    if sampling:
+        sampler.start()
     barrier(world)
     torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
         o, l = step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
     barrier(world)
+    rows = sampler.stop() if sampling else []
+    clocks = ClockSampler.summarise(rows, t_wall0, t_wall1) if rows else None
     max_s = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
     value = flops * args.steps / max_s / 1e12
 
@@ -682,8 +691,8 @@ def run_gpu_shifted(args):
             "gpu_launches": args.steps * (n_patch + max(0, n_patch - 1)),
             "e2e": {"value": round(flops * e_steps / e_s / 1e12, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e_steps},
-            "roofline": None, "cpu_baseline": None,
-            "note": "rank 0's line; the per-rank causal work is uneven (rank i runs i + 1 of the %d shards)"
+            "roofline": None, "cpu_baseline": None, "clocks": clocks,
+            "note": "rank 0's line (clocks: rank 0's GPU); the per-rank causal work is uneven (rank i runs i + 1 of the %d shards)"
                     % world if causal else "rank 0's line",
         }
         print(json.dumps(line), flush=True)
