@@ -579,3 +579,35 @@ def test_random_shapes_all_paths(m, cfg):
     o16, l16 = m.mercury_attn_sharded_bf16(q.cuda(), k.cuda(), v.cuda(), R, shift, causal)
     m.mercury_sync_status()
     assert_close(o16.float().cpu().numpy(), l16.cpu().numpy(), o_ref, l_ref, "bf16 O")
+
+
+# ---------------------------------------- shift-table capacity (R <= 32 / R > 32)
+
+@pytest.mark.parametrize("cfg", [
+    # B, Hq, Hkv, Sq, Skv, d, R, shift, causal
+    (1, 4, 2, 31 * 24, 31 * 24, 128, 31, 1, True),    # prime R: flat or unshifted only
+    (1, 4, 2, 31 * 16, 31 * 40, 64, 31, 0, False),
+    (1, 4, 4, 32 * 24, 32 * 24, 64, 32, 8, True),     # the small table's last R, nested 4 x 8
+    (1, 4, 1, 32 * 16, 32 * 48, 128, 32, 1, False),
+    (1, 4, 2, 33 * 24, 33 * 24, 128, 33, 11, True),   # the large table's first R, nested 3 x 11
+    (2, 2, 2, 33 * 16, 33 * 16, 64, 33, 1, False),
+    (1, 8, 2, 48 * 16, 48 * 16, 128, 48, 6, True),    # nested 8 x 6
+    (1, 4, 1, 64 * 8, 64 * 32, 64, 64, 16, False),    # nested 4 x 16
+], ids=lambda c: "x".join(map(str, c)))
+def test_shift_table_capacity_boundary(m, cfg, monkeypatch):
+    """Calls with R <= 32 carry a 32 x 32 shift table in the kernel
+    parameters, larger R the full one: on both sides of the switch the fused
+    path, the per-step partials (each slot against the oracle's) and a split
+    into runs equal plain attention on every row."""
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 29)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "fused")
+    op, lp, out, lse = run_partial_merge(m, q, k, v, R, shift, causal)
+    op_ref, lp_ref = oracle.attn_partial(q, k, v, R, shift, causal)
+    assert_close(op, lp, op_ref, lp_ref, "partials")
+    assert_close(out, lse, o_ref, l_ref, "partials + merge")
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "3")
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "split into 3 runs")
