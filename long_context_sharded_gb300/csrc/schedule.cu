@@ -13,12 +13,12 @@
 
 #include <algorithm>
 #include <array>
+#include <limits>
 #include <map>
 #include <mutex>
 #include <stdio.h>
 #include <stdlib.h>
 #include <string>
-#include <queue>
 #include <vector>
 
 #include "internal.h"
@@ -169,36 +169,33 @@ double launch_estimate(const Geom &g, const int *order, const mercury_cost_profi
     const long long grid = std::min<long long>(n, p.n_sms);
     if (g.causal && n > grid) {
         ItemCosts ic(g, order, p);
-        // Min-heap of (busy until, CTA): the next item goes to its root, whose
-        // time then only grows, so one sift-down restores the heap.  All CTAs
-        // start free at 0 in index order, which is already a heap.
-        using Slot = std::pair<double, long long>;
-        std::vector<Slot> heap((size_t)grid);
-        for (long long c = 0; c < grid; ++c)
-            heap[(size_t)c] = Slot(0.0, c);
+        // Winner tree over the CTAs: leaf c holds CTA c's busy-until time and
+        // every inner node the CTA of its subtree that is free earliest (ties:
+        // the lower index, which is always the left child's side).  The next
+        // item goes to the root's CTA; only the path from that leaf up changes.
+        // Padding leaves stay busy forever.
+        int L = 1;
+        while (L < grid)
+            L <<= 1;
+        std::vector<double> busy((size_t)L, std::numeric_limits<double>::infinity());
+        std::vector<int> win(2 * (size_t)L);
+        for (int c = 0; c < L; ++c) {
+            if (c < grid)
+                busy[(size_t)c] = 0.0;
+            win[(size_t)(L + c)] = c;
+        }
+        auto better = [&](int a, int b) { return busy[(size_t)b] < busy[(size_t)a] ? b : a; };
+        for (int k = L - 1; k >= 1; --k)
+            win[(size_t)k] = better(win[(size_t)(2 * k)], win[(size_t)(2 * k + 1)]);
         double last = 0.0;
         for (long long i = 0; i < n; ++i) {
             const double c = ic.next(i);
-            Slot s = heap[0];
-            s.first += c;
-            last = std::max(last, s.first);
-            size_t k = 0;
-            for (;;) {
-                const size_t l = 2 * k + 1, r = l + 1;
-                size_t m = k;
-                const Slot *best = &s;
-                if (l < heap.size() && heap[l] < *best) {
-                    m = l;
-                    best = &heap[l];
-                }
-                if (r < heap.size() && heap[r] < *best)
-                    m = r;
-                if (m == k)
-                    break;
-                heap[k] = heap[m];
-                k = m;
-            }
-            heap[k] = s;
+            const int cta = win[1];
+            const double t = busy[(size_t)cta] + c;
+            busy[(size_t)cta] = t;
+            last = std::max(last, t);
+            for (int k = (L + cta) >> 1; k >= 1; k >>= 1)
+                win[(size_t)k] = better(win[(size_t)(2 * k)], win[(size_t)(2 * k + 1)]);
         }
         return p.launch_us + std::max(last, traffic_floor_us(g, p));
     }
