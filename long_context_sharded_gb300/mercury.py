@@ -188,7 +188,7 @@ def _check_shape(t, shape, what):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch tensor" % what)
-    if tuple(t.shape) != tuple(int(x) for x in shape):
+    if t.shape != shape:  # torch.Size is a tuple
         raise ValueError("%s must have shape %s (got %s)" % (what, tuple(int(x) for x in shape),
                                                             tuple(t.shape)))
 
