@@ -611,3 +611,39 @@ def test_shift_table_capacity_boundary(m, cfg, monkeypatch):
     monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "3")
     out, lse = run_sharded(m, q, k, v, R, shift, causal)
     assert_close(out, lse, o_ref, l_ref, "split into 3 runs")
+
+
+def _random_large_r_shapes(n, seed):
+    """Seeded shapes with many virtual ranks (R from 12 to 96, on both sides
+    of the shift table's 32-rank capacity): short blocks and shards, every
+    shift form R admits, GQA groups, causal only with Sq <= Skv."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        R = int(rng.choice([12, 16, 24, 40, 48, 56, 64, 80, 96]))
+        d = int(rng.choice([64, 128]))
+        Hkv = int(rng.choice([1, 2]))
+        G = int(rng.choice([1, 2, 4]))
+        Sq = R * int(rng.integers(2, 24))
+        Skv = Sq if rng.random() < 0.5 else R * int(rng.integers(2, 48))
+        causal = bool(rng.random() < 0.5) and Sq <= Skv
+        shifts = [0, 1] + [k for k in range(2, R) if R % k == 0]
+        shift = int(rng.choice(shifts))
+        out.append((1, Hkv * G, Hkv, Sq, Skv, d, R, shift, causal))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _random_large_r_shapes(10, 2027), ids=lambda c: "x".join(map(str, c)))
+def test_random_large_r_all_paths(m, cfg, monkeypatch):
+    """Fused, per-step partials + merge and a split into runs on a seeded
+    shape with many virtual ranks, every row against the oracle."""
+    B, Hq, Hkv, Sq, Skv, d, R, shift, causal = cfg
+    q, k, v = make_qkv(B, Hq, Hkv, Sq, Skv, d, seed=sum(cfg[:7]) + 17)
+    o_ref, l_ref = oracle.attn(q, k, v, causal)
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "fused")
+    _, _, out, lse = run_partial_merge(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "partials + merge")
+    monkeypatch.setenv("MERCURY_SPLIT_GROUPS", "5")
+    out, lse = run_sharded(m, q, k, v, R, shift, causal)
+    assert_close(out, lse, o_ref, l_ref, "split into 5 runs")
